@@ -1,0 +1,364 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused mHC boundary (n_hc = 4) on GB300.
+
+A step is one shifted fused boundary call (residual update, sums of squares,
+mixer contraction, coefficients, collapse and layer RMSNorm) over the
+prefill workload: 8192 tokens, hidden 7168, with every input resident in HBM
+when the timed region starts. Per step the inputs (1.18 GB) are far larger
+than L2 (129 MB), so no flush is needed; the prepared mixer (2.75 MB) stays
+L2-resident as it does in a serving loop.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle instead
+(this build has no other reference implementation), on a bounded sample of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "mHC boundary tokens/s and achieved HBM GB/s (% of GB300 peak), hidden 7168"
+WORKLOAD = "prefill_t8192_h7168"
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def alg_bytes_call(T: int, H: int) -> int:
+    """Algorithmic bytes of one shifted fused boundary call: residual read and
+    write (8H each), x read and layer input write (2H each), 96 B of
+    coefficients in and 96 B out per token; the prepared mixer (384H) and the
+    fp32 norm weight (4H) once."""
+    return T * (20 * H + 192) + 388 * H
+
+
+def alg_bytes_stream_kernel(T: int, H: int) -> int:
+    """Algorithmic bytes of the streaming kernel: residual, x and 96 B of
+    coefficients read, updated residual and collapse written, per token; the
+    prepared mixer once."""
+    return T * (20 * H + 96) + 384 * H
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only)
+    every few milliseconds while running."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_dev: int):
+        self.samples, self.reasons, self.max_mhz, self.ok = [], set(), None, False
+        self._stop = threading.Event()
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(torch_dev)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self.nv, self.h, self.ok = nv, h, True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": 0}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------- oracle timing
+
+
+def time_oracle(T_sample: int, H: int, seed: int, budget_s: float, chunk: int = 32):
+    """The oracle as it stands, on fresh seeded tokens of the workload's
+    distribution, single-threaded; stops after `budget_s` or `T_sample`
+    tokens. Returns (tokens, seconds)."""
+    import oracle as orc
+    from manifold_constrained_hyper_gb300 import synth
+    d = synth.make_inputs(min(chunk, T_sample), H, seed)
+    done, t0 = 0, time.perf_counter()
+    while done < T_sample and time.perf_counter() - t0 < budget_s:
+        orc.boundary(orc.MODE_FUSED_SHIFTED, d["residual"], d["fn"], d["scale"], d["base"],
+                     d["norm_w"], x=d["x"], post_mix=d["post"], comb=d["comb"],
+                     pre_lag=d["pre_lag"])
+        done += d["residual"].shape[0]
+    return done, time.perf_counter() - t0
+
+
+# ---------------------------------------------------------------- arms
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    from manifold_constrained_hyper_gb300 import synth
+    import oracle as orc
+    orc.build_oracle()
+    cfg = synth.WORKLOADS[args.workload]
+    H = cfg["H"]
+    per_step = args.reference_tokens
+    for _ in range(args.warmup):
+        time_oracle(min(per_step, 8), H, cfg["seed"], 1e9, chunk=min(per_step, 8))
+    total_tok, total_s = 0, 0.0
+    for _ in range(args.steps):
+        n, s = time_oracle(per_step, H, cfg["seed"], 1e9, chunk=per_step)
+        total_tok += n
+        total_s += s
+    v = total_tok / total_s
+    sample = (f"{per_step} tokens per step of the {args.workload} workload (H={H}), "
+              f"single-threaded C oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "tokens": cfg["T"], "hidden": H, "n_hc": 4,
+                   "variant": "shifted fused boundary"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from manifold_constrained_hyper_gb300 import build as mbuild
+    from manifold_constrained_hyper_gb300 import ops, synth
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    if rank == 0 or not os.path.exists(ops.lib_path()):
+        mbuild.build()
+    if world > 1:
+        dist.barrier()
+    ops.load()
+    dev = torch.device("cuda", local)
+    cfg = synth.WORKLOADS[args.workload]
+    T, H = cfg["T"], cfg["H"]
+    extra = {k: v for k, v in cfg.items() if k not in ("T", "H", "seed")}
+    d = synth.make_inputs_device(T, H, cfg["seed"] + 7919 * rank, dev, **extra)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    res, x = d["residual_dev"], d["x_dev"]
+    post, comb, pre_lag = f32(d["post"]), f32(d["comb"]), f32(d["pre_lag"])
+    scale, base, nw = f32(d["scale"]), f32(d["base"]), f32(d["norm_w"])
+    w = ops.mhc_prepare_weight(f32(d["fn"]))
+    params = ops.Params(sinkhorn_iters=20)
+    ro = torch.empty_like(res)
+    li = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    pr = torch.empty(T, 4, device=dev)
+    po = torch.empty(T, 4, device=dev)
+    cb = torch.empty(T, 4, 4, device=dev)
+    ws = torch.empty(max(ops.workspace_bytes(T, H), 16), dtype=torch.uint8, device=dev)
+
+    def step(between=None):
+        if between is not None:
+            ops.mhc_debug_record_between(between)
+        ops.mhc_boundary_fused(x, res, post, comb, w, scale, base, nw, pre_lag, params,
+                               residual_out=ro, layer_input=li, pre_out=pr, post_out=po,
+                               comb_out=cb, workspace=ws)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if ops.mhc_get_device_status() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    K = args.steps
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_begin.record()
+        for i in range(K):
+            ev_s[i].record()
+            step(ev_m[i])
+            ev_e[i].record()
+        t_end.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    status = ops.mhc_get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    total_ms = t_begin.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    stream_ms = statistics.mean(ev_s[i].elapsed_time(ev_m[i]) for i in range(K))
+    finish_ms = statistics.mean(ev_m[i].elapsed_time(ev_e[i]) for i in range(K))
+    ms_per_step = total_ms / K
+    value = world * T * K / (total_ms / 1e3)
+    peak, peak_kind = measured_peaks()
+    gbps_call = alg_bytes_call(T, H) / (ms_per_step / 1e3) / 1e9
+    ach = alg_bytes_stream_kernel(T, H) / (stream_ms / 1e3) / 1e9
+
+    # ---------------- end to end: host buffers through the public API
+    e2e = None
+    if not args.no_e2e:
+        hres = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
+        hres.copy_(res)
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hx.copy_(x)
+        hsmall = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+                  for t in (post, comb, pre_lag)]
+        houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (ro, li, pr, po, cb)]
+        dres, dx = torch.empty_like(res), torch.empty_like(x)
+        dsmall = [torch.empty_like(t) for t in (post, comb, pre_lag)]
+        h2d = sum(t.numel() * t.element_size() for t in [hres, hx] + hsmall)
+        d2h = sum(t.numel() * t.element_size() for t in houts)
+
+        def e2e_step():
+            dres.copy_(hres, non_blocking=True)
+            dx.copy_(hx, non_blocking=True)
+            for dd, hh in zip(dsmall, hsmall):
+                dd.copy_(hh, non_blocking=True)
+            ops.mhc_boundary_fused(dx, dres, dsmall[0], dsmall[1], w, scale, base, nw, dsmall[2],
+                                   params, residual_out=ro, layer_input=li, pre_out=pr,
+                                   post_out=po, comb_out=cb, workspace=ws)
+            for hh, dd in zip(houts, (ro, li, pr, po, cb)):
+                hh.copy_(dd, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        K2 = max(1, min(K, args.e2e_steps))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(K2):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": world * T * K2 / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, s = time_oracle(T, H, cfg["seed"], args.cpu_seconds)
+        cpu = {"value": n / s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} tokens of the {args.workload} distribution in {s:.1f} s, "
+                         f"single-threaded C oracle, chunks of 32 tokens"}
+
+    S, sw = ops.plan(T, H)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; residual/x ~ N(0,1) bf16, doubly stochastic comb)",
+        "config": {"workload": args.workload, "tokens": T, "hidden": H, "n_hc": 4,
+                   "variant": "shifted fused boundary", "sinkhorn_iters": 20,
+                   "norm_w": "fp32", "hidden_slices": S, "slice_width": sw,
+                   "l2": "inputs larger than L2 (no flush); prepared mixer L2-resident",
+                   "parallelism": f"replicas x{world} (token-sharded, no collective)"},
+        "achieved_gbps": gbps_call,
+        "achieved_frac_of_peak": gbps_call / peak,
+        "kernel_ms": {"stream": stream_ms, "finish": finish_ms},
+        "roofline": {"bound": "hbm", "kernel": "stream_kernel", "achieved": ach, "peak": peak,
+                     "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                     "peak_source": peak_kind},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-tokens", type=int, default=256)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,208 @@
+/*
+ * mhc.h: C ABI of the GB300 (sm_103a) mHC layer boundary, n_hc = 4.
+ *
+ * The boundary between layer l and l+1 of a manifold-constrained
+ * hyper-connection stack, per token (X_{l+1} = B_l X_l + C_l F_l(A_l X_l),
+ * "The Hyper Connection Preprocessing GPU Kernel Study", section "why this
+ * kernel is called pre"):
+ *   post  (residual update): residual'[s] = bf16(post[s]*x + sum_j comb[j][s]*residual[j])
+ *   pre   (coefficients and layer input of the next layer): sum of squares of
+ *         the flattened 4H residual -> rstd; 24 mixes = TF32(fn) . residual;
+ *         pre = sigmoid(..)+eps, post = 2 sigmoid(..), comb = Sinkhorn(softmax(..));
+ *         layer_input = bf16(bf16(sum_j pre[j]*residual[j]) * rstd_li * norm_w).
+ * The fused entry point does both in one pass over the residual; its shifted
+ * form collapses with the previous boundary's pre ("vllm.models.deepseek_v41
+ * .nvidia.ops.mhc_boundary", mhc_shifted_post_pre_boundary).
+ *
+ * Conventions for every entry point below.
+ *   - Tensors are plain, contiguous, row-major buffers. "bf16" buffers hold
+ *     bfloat16 bit patterns as uint16_t. Unless stated otherwise a pointer is a
+ *     DEVICE pointer on the current CUDA device, owned by the caller; the
+ *     library never frees or retains it past the call.
+ *   - Every pointer must be 16-byte aligned (MHC_ERR_ALIGN otherwise).
+ *   - tokens T >= 0 (T == 0 is a no-op returning MHC_OK); hidden H must be a
+ *     multiple of 32 in [32, 65536] (MHC_ERR_UNSUPPORTED otherwise).
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued asynchronously; argument errors are returned before
+ *     anything is enqueued. A launch failure returns MHC_ERR_CUDA.
+ *   - No entry point allocates device memory. Scratch space, where needed, is
+ *     the caller's `workspace` (see mhc_workspace_bytes).
+ *   - Device-side waits are bounded: a kernel whose wait runs out records
+ *     MHC_ERR_DEVICE_TIMEOUT in a per-device status word and returns early;
+ *     read it with mhc_get_device_status().
+ *   - Outputs must not overlap inputs or each other, except that
+ *     residual_out may be exactly the residual buffer (in-place update).
+ *     Partial overlap returns MHC_ERR_ALIAS.
+ *   - Entry points are thread-safe; results are deterministic run to run
+ *     for a given (T, H) (fixed reduction order).
+ */
+#ifndef MHC_H
+#define MHC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHC_OK = 0,
+    MHC_ERR_NULL = 1,           /* a required pointer is NULL */
+    MHC_ERR_ALIGN = 2,          /* a pointer is not 16-byte aligned */
+    MHC_ERR_SHAPE = 3,          /* negative T, bad params (sinkhorn_iters < 1) */
+    MHC_ERR_UNSUPPORTED = 4,    /* H outside the supported set, or not an sm_103 device */
+    MHC_ERR_ALIAS = 5,          /* an output overlaps an input or another output */
+    MHC_ERR_CUDA = 6,           /* a CUDA runtime/driver call failed */
+    MHC_ERR_DEVICE_TIMEOUT = 7, /* a device-side bounded wait ran out */
+    MHC_ERR_WORKSPACE = 8       /* workspace NULL or smaller than mhc_workspace_bytes */
+} mhc_status;
+
+/* Scalar parameters of a boundary ("mhc_boundary" page, mhc_shifted_post_pre_boundary
+ * arguments hc_norm_eps, hc_pre_eps, hc_post_scale, sinkhorn_eps,
+ * num_sinkhorn_iters, norm_eps). */
+typedef struct {
+    float hc_norm_eps;   /* eps inside rstd = rsqrt(ssq / (4H) + hc_norm_eps) */
+    float hc_pre_eps;    /* pre = sigmoid(.) + hc_pre_eps */
+    float hc_post_mult;  /* post = sigmoid(.) * hc_post_mult (2 in DeepSeek) */
+    float sinkhorn_eps;  /* softmax floor and Sinkhorn denominator eps */
+    float norm_eps;      /* eps of the layer RMSNorm of the collapse (over H) */
+    int sinkhorn_iters;  /* >= 1: one column step, then iters-1 (row, column) steps */
+} mhc_params;
+
+/* Element type of norm_w. The DeepSeek boundary kernel reads bf16 weights;
+ * fp32 is the common checkpoint dtype. */
+typedef enum { MHC_F32 = 0, MHC_BF16 = 1 } mhc_dtype;
+
+/* ---------------------------------------------------------------------- */
+/* Weight preparation ("mhc_boundary" page, prepare_boundary_weight).       */
+
+/* Bytes of the prepared mixer for hidden H: 48 rows x 4H bf16 = 384*H. */
+size_t mhc_weight_bytes(int hidden);
+
+/*
+ * fn: [24, 4H] fp32, rows 0-3 pre, 4-7 post, 8-23 comb (row-major 4x4),
+ *     column s*H + h multiplies stream s, hidden h of the residual.
+ * weight: output, mhc_weight_bytes(H) bytes, 16-byte aligned.
+ *
+ * Each weight w is rounded to TF32 (round half away from zero on the bit
+ * pattern: r = (bits(w) + 0x1000) & ~0x1FFF) and split into two bf16 parts,
+ * hi = bf16_rne(r) and lo = bf16_rne(r - hi), with hi + lo == r exactly, so
+ * BF16 tensor-core products reproduce TF32 products exactly. Layout (uint16
+ * units): stacked row r in [0, 48) holds hi of mix r (r < 24) or lo of mix
+ * r - 24; for hidden chunk c in [0, H/32), stream s and element e in [0, 32)
+ * the value for column k = s*H + 32c + e is at
+ *     ((c*4 + s)*48 + r)*32 + 8*((e/8) ^ ((r/2) % 4)) + (e % 8),
+ * i.e. per (chunk, stream) a 48 x 64-byte tile, K-major, in the 64-byte
+ * swizzled order the tensor cores read from shared memory.
+ * Inputs must be finite (NaN payloads are not preserved by the rounding).
+ */
+mhc_status mhc_prepare_weight(const float *fn, int hidden, void *weight, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Residual update alone ("mhc_boundary" page, residual_update).            */
+
+/*
+ * x: [T, H] bf16 layer output; residual: [T, 4, H] bf16; post: [T, 4] fp32;
+ * comb: [T, 4, 4] fp32 where comb[t][j][s] carries stream j into stream s.
+ * residual_out: [T, 4, H] bf16 (may be == residual).
+ *   residual_out[t][s][h] = bf16_rne(chain), chain = post[s]*x[h], then
+ *   fma(comb[j][s], residual[j][h], chain) for j = 0..3, every operand and
+ *   result of the chain flushed to zero when subnormal.
+ */
+mhc_status mhc_post(const uint16_t *x, const uint16_t *residual, const float *post,
+                    const float *comb, uint16_t *residual_out, int64_t tokens,
+                    int hidden, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Pre and fused boundary.                                                  */
+
+/* Bytes of caller-provided device scratch for mhc_pre / mhc_boundary_fused
+ * at (T, H): per-token partial mixes and sums of squares of every hidden
+ * slice. 0 when T == 0. */
+size_t mhc_workspace_bytes(int64_t tokens, int hidden);
+
+/*
+ * Unshifted pre ("The Hyper Connection Preprocessing GPU Kernel Study",
+ * mhc_pre_big_fuse with the in-kernel square sum; mixes computed in-kernel).
+ * residual: [T, 4, H] bf16. weight: from mhc_prepare_weight(fn, H).
+ * scale: [3] fp32 (pre, post, comb). base: [24] fp32 (rows of fn).
+ * norm_w: [H] of norm_dtype, or NULL to write the raw collapse.
+ * Outputs: layer_input [T, H] bf16, pre_out [T, 4], post_out [T, 4],
+ * comb_out [T, 4, 4] fp32.
+ *   ssq = sum over the 4H values of residual^2, rstd = rsqrt(ssq/(4H) + hc_norm_eps)
+ *   mix[n] = sum_k TF32(fn[n][k]) * residual_flat[k]        (fp32 accumulate)
+ *   pre[i] = sigmoid(fma(mix[i]*rstd, scale[0], base[i])) + hc_pre_eps
+ *   post[i] = sigmoid(fma(mix[4+i]*rstd, scale[1], base[4+i])) * hc_post_mult
+ *   comb = Sinkhorn of row softmax of fma(mix[8+4i+k]*rstd, scale[2], base[8+4i+k])
+ *          (entries fma(e, 1/sum e, sinkhorn_eps)), sigmoid(v) = 1/min(1+exp(-v), 2^126)
+ *   li[h] = bf16(fma chain of pre[j]*residual[j][h]), rstd_li = rsqrt(sum li^2 / H + norm_eps)
+ *   layer_input[h] = bf16((li[h]*rstd_li) * norm_w[h])   (li itself when norm_w == NULL)
+ * workspace: device scratch of at least mhc_workspace_bytes(T, H) bytes.
+ */
+mhc_status mhc_pre(const uint16_t *residual, const void *weight, const float *scale,
+                   const float *base, const void *norm_w, mhc_dtype norm_dtype,
+                   const mhc_params *params, int64_t tokens, int hidden,
+                   uint16_t *layer_input, float *pre_out, float *post_out,
+                   float *comb_out, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
+ * Fused post + pre boundary ("mhc_boundary" page, mhc_shifted_post_pre_boundary
+ * and MhcBoundaryKernel): the residual update of mhc_post, then the pre of
+ * mhc_pre computed on the UPDATED residual, in one pass over the residual.
+ * pre_lag: [T, 4] fp32 pre of the previous boundary (shifted form: the layer
+ * input collapses the updated residual with pre_lag), or NULL (unshifted
+ * form: it collapses with this boundary's own pre_out).
+ * Other arguments as in mhc_post and mhc_pre. residual_out may be == residual.
+ */
+mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
+                              const float *post, const float *comb,
+                              const float *pre_lag, const void *weight,
+                              const float *scale, const float *base,
+                              const void *norm_w, mhc_dtype norm_dtype,
+                              const mhc_params *params, int64_t tokens, int hidden,
+                              uint16_t *residual_out, uint16_t *layer_input,
+                              float *pre_out, float *post_out, float *comb_out,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Status and diagnostics.                                                  */
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns MHC_OK, MHC_ERR_DEVICE_TIMEOUT (a kernel's bounded wait ran
+ * out since the last read) or MHC_ERR_CUDA. */
+mhc_status mhc_get_device_status(void *stream);
+
+/* Extra detail of the last timeout read by mhc_get_device_status: the wait
+ * site id (0 if none). */
+int mhc_last_timeout_site(void);
+
+/* Human-readable name of a status. Static storage; never NULL. */
+const char *mhc_status_string(mhc_status status);
+
+/* Limit of every device-side wait, in nanoseconds (default 1e9 = 1 s).
+ * Applies to launches enqueued after the call. ns == 0 restores the default. */
+void mhc_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook for the bounded-wait machinery: launches one CTA that waits on a
+ * shared-memory barrier nothing ever arrives at, under the current limit,
+ * so that the wait runs out and the kernel returns. Enqueued on `stream`;
+ * read the outcome with mhc_get_device_status(). */
+mhc_status mhc_debug_unarmed_wait(void *stream);
+
+/* Benchmark hook: the next mhc_pre / mhc_boundary_fused call made by this
+ * host thread records `event` (a cudaEvent_t passed as void*) on its stream
+ * right after its streaming kernel and before its finishing kernel, so that
+ * the two kernels can be timed apart with events. Consumed by that call;
+ * NULL clears a pending event. */
+void mhc_debug_record_between(void *event);
+
+/* Slice plan chosen for (T, H): writes the number of hidden slices and the
+ * slice width. For tests and the benchmark's byte accounting. */
+mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MHC_H */

@@ -1,0 +1,357 @@
+// Weight preparation, the standalone residual update, the finishing kernels
+// of the boundary (slice reduction, coefficients with a warp-shuffle
+// Sinkhorn, layer RMSNorm of the collapse), the device status word and the
+// wait-timeout probe.
+#include <cuda_bf16.h>
+
+#include "mhc_internal.h"
+#include "ptx.cuh"
+
+namespace mhc {
+
+__device__ unsigned int g_status_word;
+
+namespace {
+
+// ------------------------------------------------------------ weight prep
+// One thread per (chunk c, stream s, stacked row r, 8-wide unit u): TF32
+// rounding (half away from zero on the bit pattern), exact bf16 hi/lo split
+// ("mhc_boundary" page, prepare_boundary_weight), written to the 64-byte
+// swizzled position of the (c, s) tile.
+__global__ void prepare_weight_kernel(const float *__restrict__ fn, int H,
+                                      uint8_t *__restrict__ out) {
+    const long long total = static_cast<long long>(H / kChunk) * 4 * kWRows * 4;
+    const long long K = 4LL * H;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int u = static_cast<int>(i % 4);
+        const int r = static_cast<int>((i / 4) % kWRows);
+        const int s = static_cast<int>((i / (4 * kWRows)) % 4);
+        const long long c = i / (4 * kWRows * 4);
+        const int row = r % 24;
+        const bool lo_part = r >= 24;
+        const long long k0 = static_cast<long long>(s) * H + c * kChunk + 8 * u;
+        const float4 *src = reinterpret_cast<const float4 *>(fn + row * K + k0);
+        const float4 a = src[0], b = src[1];
+        const float w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float rt = __uint_as_float((__float_as_uint(w[e]) + 0x1000u) & 0xFFFFE000u);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(rt);
+            if (!lo_part) {
+                h[e] = __bfloat16_as_ushort(hi);
+            } else {
+                const float rest = __fsub_rn(rt, __bfloat162float(hi));
+                h[e] = __bfloat16_as_ushort(__float2bfloat16_rn(rest));
+            }
+        }
+        const uint4 v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                   h[6] | (h[7] << 16));
+        const long long tile = c * 4 + s;
+        uint4 *dst = reinterpret_cast<uint4 *>(out + (tile * kWRows + r) * kRowBytes +
+                                               16 * (u ^ ((r >> 1) & 3)));
+        *dst = v;
+    }
+}
+
+// ------------------------------------------------------------ residual update
+// Standalone post ("mhc_boundary" page, residual_update): one thread per
+// (token, 8-wide hidden unit), 16-byte loads and stores, coefficients through
+// the read-only path.
+__global__ void post_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ res,
+                            const float *__restrict__ post, const float *__restrict__ comb,
+                            uint16_t *out, long long T, int H) {
+    const int units = H / 8;
+    const long long total = T * units;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long t = i / units;
+        const int u = static_cast<int>(i % units);
+        const float4 pv = __ldg(reinterpret_cast<const float4 *>(post) + t);
+        float4 cv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cv[j] = __ldg(reinterpret_cast<const float4 *>(comb) + t * 4 + j);
+        uint4 r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            r[j] = ld_global_nc_v4(res + (t * 4 + j) * H + 8LL * u);
+        const uint4 xw = ld_global_nc_v4(x + t * H + 8LL * u);
+        const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w};
+        const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const float cs[4] = {(&cv[0].x)[s], (&cv[1].x)[s], (&cv[2].x)[s], (&cv[3].x)[s]};
+            uint32_t w[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint64_t nu = mul2_ftz(f2_pack(ps[s], ps[s]), bf2_unpack(xs[p]));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t rw = (&r[j].x)[p];
+                    nu = fma2_ftz(f2_pack(cs[j], cs[j]), bf2_unpack(rw), nu);
+                }
+                w[p] = bf2_pack_rn(nu);
+            }
+            *reinterpret_cast<uint4 *>(out + (t * 4 + s) * H + 8LL * u) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// ------------------------------------------------------------ coefficients
+__device__ __forceinline__ float sigmoid_clamped(float v) {
+    // 1 / min(1 + exp(-v), 2^126) ("mhc_boundary" page, sigmoid)
+    return __frcp_rn(fminf(1.0f + expf(-v), 0x1p126f));
+}
+
+// Lane map of one token's warp: lanes 0-3 pre (mix 0-3), 4-7 post (mix 4-7),
+// lane 8 the 4H sum of squares, lane 9 the collapse's sum of squares, lanes
+// 16-31 comb (mix 8-23, lane 16 + 4i + k = row i, column k).
+__device__ __forceinline__ int lane_slot(int lane) {
+    if (lane < 8) return lane;
+    if (lane == 8) return 24;
+    if (lane == 9) return 25;
+    if (lane >= 16) return lane - 8;
+    return -1;
+}
+
+// Sum of one token's slice partials in slice order (fixed, deterministic).
+__device__ __forceinline__ float reduce_slices(const float *__restrict__ partials, int n_slices,
+                                               long long T, long long t, int slot) {
+    float v = 0.f;
+    if (slot >= 0) {
+        const float *p = partials + t * kPartStride + slot;
+        const long long step = T * kPartStride;
+        for (int s = 0; s < n_slices; ++s) v += __ldg(p + s * step);
+    }
+    return v;
+}
+
+// Coefficients of token t from its reduced value v (lane map above); writes
+// pre / post / comb. Returns pre[lane & 3] in lanes 0-3 (undefined elsewhere).
+// Order of operations as in the "mhc_boundary" page (coefficients, sinkhorn,
+// col_normalize); the Sinkhorn runs on 16 lanes with shuffles.
+__device__ float coefficients_warp(float v, int lane, const CoefArgs &c, int H, long long t,
+                                   float *pre_out, float *post_out, float *comb_out) {
+    const unsigned full = 0xffffffffu;
+    const float ssq = __shfl_sync(full, v, 8);
+    const float rstd = rsqrtf(__fdiv_rn(ssq, static_cast<float>(4 * H)) + c.hc_norm_eps);
+    const int slot = lane_slot(lane);
+    const float m = v * rstd;
+    float pre = 0.f;
+    if (lane < 4) {
+        pre = sigmoid_clamped(fmaf(m, __ldg(c.scale + 0), __ldg(c.base + slot))) + c.hc_pre_eps;
+        pre_out[t * 4 + lane] = pre;
+    } else if (lane < 8) {
+        const float p = sigmoid_clamped(fmaf(m, __ldg(c.scale + 1), __ldg(c.base + slot)));
+        post_out[t * 4 + lane - 4] = p * c.hc_post_mult;
+    }
+    // comb lanes 16..31; the other lanes follow the shuffles on dummy values
+    const bool comb_lane = lane >= 16;
+    const float l = comb_lane ? fmaf(m, __ldg(c.scale + 2), __ldg(c.base + slot)) : 0.f;
+    const int rb = lane & ~3;   // first lane of this row
+    float mx = fmaxf(l, __shfl_xor_sync(full, l, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(full, mx, 2));
+    const float e = comb_lane ? expf(l - mx) : 1.f;
+    const float e0 = __shfl_sync(full, e, rb), e1 = __shfl_sync(full, e, rb + 1);
+    const float e2 = __shfl_sync(full, e, rb + 2), e3 = __shfl_sync(full, e, rb + 3);
+    const float inv = __frcp_rn(((e0 + e1) + e2) + e3);
+    const float eps = c.sinkhorn_eps;
+    float x = fmaf(e, inv, eps);
+    // column normalisation: (c0k + c1k) + (c2k + c3k), plus eps
+    float cs = x + __shfl_xor_sync(full, x, 4);
+    cs = cs + __shfl_xor_sync(full, cs, 8);
+    x = x * __frcp_rn(cs + eps);
+    for (int it = 1; it < c.sinkhorn_iters; ++it) {
+        const float c0 = __shfl_sync(full, x, rb), c1 = __shfl_sync(full, x, rb + 1);
+        const float c2 = __shfl_sync(full, x, rb + 2), c3 = __shfl_sync(full, x, rb + 3);
+        x = x * __frcp_rn((((c0 + c1) + c2) + c3) + eps);
+        cs = x + __shfl_xor_sync(full, x, 4);
+        cs = cs + __shfl_xor_sync(full, cs, 8);
+        x = x * __frcp_rn(cs + eps);
+    }
+    if (comb_lane) comb_out[t * 16 + (lane - 16)] = x;
+    return pre;
+}
+
+// out = bf16((li * rstd_li) * norm_w) for 8 values
+__device__ __forceinline__ uint4 norm8(uint4 li, float rstd_li, const void *norm_w, int nw_bf16,
+                                       long long h) {
+    float w[8];
+    if (nw_bf16) {
+        const uint4 nv = ld_global_nc_v4(static_cast<const uint16_t *>(norm_w) + h);
+        const uint32_t ws[4] = {nv.x, nv.y, nv.z, nv.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            w[2 * p] = __uint_as_float(ws[p] << 16);
+            w[2 * p + 1] = __uint_as_float(ws[p] & 0xFFFF0000u);
+        }
+    } else {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(norm_w) + h));
+        const float4 b =
+            __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(norm_w) + h) + 1);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    }
+    const uint32_t ls[4] = {li.x, li.y, li.z, li.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float lo = __fmul_rn(__fmul_rn(__uint_as_float(ls[p] << 16), rstd_li), w[2 * p]);
+        const float hi =
+            __fmul_rn(__fmul_rn(__uint_as_float(ls[p] & 0xFFFF0000u), rstd_li), w[2 * p + 1]);
+        o[p] = bf2_pack_rn(f2_pack(lo, hi));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ------------------------------------------------------------ finish (shifted)
+// One warp per token: slice reduction, coefficients, then the RMSNorm of the
+// collapse the streaming pass left (unnormalised) in layer_input.
+__global__ void __launch_bounds__(256) finish_shifted_kernel(const FinishArgs a) {
+    const int lane = threadIdx.x & 31;
+    const long long t = blockIdx.x * 8LL + (threadIdx.x >> 5);
+    if (t >= a.T) return;
+    const float v = reduce_slices(a.partials, a.n_slices, a.T, t, lane_slot(lane));
+    const float ssql = __shfl_sync(0xffffffffu, v, 9);
+    if (a.norm_w != nullptr) {
+        const float rstd_li =
+            rsqrtf(__fdiv_rn(ssql, static_cast<float>(a.H)) + a.coef.norm_eps);
+        uint16_t *row = a.layer_input + t * a.H;
+        for (int u = lane; u < a.H / 8; u += 32) {
+            const uint4 li = *reinterpret_cast<const uint4 *>(row + 8LL * u);
+            *reinterpret_cast<uint4 *>(row + 8LL * u) = norm8(li, rstd_li, a.norm_w, a.nw_bf16, 8LL * u);
+        }
+    }
+    coefficients_warp(v, lane, a.coef, a.H, t, a.pre_out, a.post_out, a.comb_out);
+}
+
+// ------------------------------------------------------------ finish (unshifted)
+// One 128-thread block per token: warp 0 reduces the slices and forms the
+// coefficients; then all threads collapse the token's 4 streams with this
+// boundary's pre into shared memory, reduce the collapse's sum of squares
+// in a fixed order, and write the normalised layer input.
+constexpr int kFinThreads = 128;
+
+__global__ void __launch_bounds__(kFinThreads) finish_unshifted_kernel(const FinishArgs a) {
+    extern __shared__ uint4 li_s[];            // [H/8]
+    __shared__ float pre_s[4];
+    __shared__ float red_s[kFinThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long t = blockIdx.x;
+    if (warp == 0) {
+        const float v = reduce_slices(a.partials, a.n_slices, a.T, t, lane_slot(lane));
+        const float pre = coefficients_warp(v, lane, a.coef, a.H, t, a.pre_out, a.post_out,
+                                            a.comb_out);
+        if (lane < 4) pre_s[lane] = pre;
+    }
+    __syncthreads();
+    const uint64_t p2[4] = {f2_pack(pre_s[0], pre_s[0]), f2_pack(pre_s[1], pre_s[1]),
+                            f2_pack(pre_s[2], pre_s[2]), f2_pack(pre_s[3], pre_s[3])};
+    const int units = a.H / 8;
+    uint64_t sq2 = 0;
+    for (int u = tid; u < units; u += kFinThreads) {
+        uint32_t cs[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 r = ld_global_nc_v4(a.cur + (t * 4 + j) * a.H + 8LL * u);
+            cs[j][0] = r.x; cs[j][1] = r.y; cs[j][2] = r.z; cs[j][3] = r.w;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            uint64_t acc = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc = fma2(p2[j], bf2_unpack(cs[j][p]), acc);
+            w[p] = bf2_pack_rn(acc);
+            const uint64_t lv = bf2_unpack(w[p]);
+            sq2 = fma2(lv, lv, sq2);
+        }
+        li_s[u] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    uint16_t *row = a.layer_input + t * a.H;
+    if (a.norm_w == nullptr) {
+        for (int u = tid; u < units; u += kFinThreads)
+            *reinterpret_cast<uint4 *>(row + 8LL * u) = li_s[u];
+        return;
+    }
+    float sq = f2_lo(sq2) + f2_hi(sq2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) red_s[warp] = sq;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFinThreads / 32; ++w) tot += red_s[w];
+    const float rstd_li = rsqrtf(__fdiv_rn(tot, static_cast<float>(a.H)) + a.coef.norm_eps);
+    for (int u = tid; u < units; u += kFinThreads)
+        *reinterpret_cast<uint4 *>(row + 8LL * u) =
+            norm8(li_s[u], rstd_li, a.norm_w, a.nw_bf16, 8LL * u);
+}
+
+// ------------------------------------------------------------ timeout probe
+__global__ void unarmed_wait_kernel(unsigned int *status, unsigned long long timeout_ns) {
+    __shared__ alignas(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_addr(&bar), 1);
+        fence_mbar_init();
+        // Nothing ever arrives: the bounded wait must run out and return.
+        mbar_wait(smem_addr(&bar), 0, &abort_flag, timeout_ns, status, 99);
+    }
+}
+
+}  // namespace
+
+unsigned int *device_status_word() {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    return static_cast<unsigned int *>(p);
+}
+
+cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s) {
+    const long long total = static_cast<long long>(H / kChunk) * 4 * kWRows * 4;
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    prepare_weight_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), threads, 0, s>>>(fn, H, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *post,
+                        const float *comb, uint16_t *out, long long T, int H, cudaStream_t s) {
+    const long long total = T * (H / 8);
+    const int threads = 256;
+    long long blocks = (total + threads - 1) / threads;
+    const long long cap = 152LL * 8 * 4;
+    if (blocks > cap) blocks = cap;
+    post_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(x, res, post, comb, out, T, H);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finish_shifted(const FinishArgs &a, cudaStream_t s) {
+    const long long blocks = (a.T + 7) / 8;
+    finish_shifted_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finish_unshifted(const FinishArgs &a, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(a.H) * 2;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(finish_unshifted_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    finish_unshifted_kernel<<<static_cast<unsigned>(a.T), kFinThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unarmed_wait(unsigned int *status, unsigned long long timeout_ns,
+                                cudaStream_t s) {
+    unarmed_wait_kernel<<<1, 32, 0, s>>>(status, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace mhc

@@ -1,0 +1,383 @@
+// Host side of the C ABI declared in include/mhc.h: argument validation,
+// the hidden-slice plan, TMA tensor-map encoding and kernel dispatch.
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "mhc.h"
+#include "mhc_internal.h"
+
+using namespace mhc;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kPlanSlots = 2 * 152;   // co-resident stream CTAs on a 152-SM GB300
+constexpr int kStages = 2;
+
+std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
+thread_local int t_last_site = 0;
+thread_local cudaEvent_t t_between_event = nullptr;
+
+struct DeviceInfo {
+    std::once_flag once;
+    bool ok = false;
+    unsigned int *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+mhc_status current_device(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MHC_ERR_CUDA;
+    DeviceInfo &d = g_dev[dev];
+    std::call_once(d.once, [&] {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+            return;
+        if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return;
+        if (major != 10 || minor != 3) return;   // the library carries sm_103a code only
+        d.status = device_status_word();
+        d.ok = d.status != nullptr;
+    });
+    if (!d.ok) return MHC_ERR_UNSUPPORTED;
+    *out = &d;
+    return MHC_OK;
+}
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool hidden_ok(int H) { return H >= kChunk && H <= 65536 && H % kChunk == 0; }
+
+// Half-open byte ranges [a, a + an) and [b, b + bn) intersect.
+bool overlap(const void *a, size_t an, const void *b, size_t bn) {
+    if (!a || !b || an == 0 || bn == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bn && y < x + an;
+}
+
+struct Range {
+    const void *p;
+    size_t n;
+};
+
+// Any output overlapping any input or another output, except an output
+// identical (same pointer, same size) to an input marked `may_equal`.
+bool aliasing(const Range *outs, int no, const Range *ins, int ni, const void *may_equal_in,
+              const void *may_equal_out) {
+    for (int i = 0; i < no; ++i) {
+        for (int j = 0; j < ni; ++j) {
+            if (outs[i].p == may_equal_out && ins[j].p == may_equal_in && outs[i].p == ins[j].p)
+                continue;
+            if (overlap(outs[i].p, outs[i].n, ins[j].p, ins[j].n)) return true;
+        }
+        for (int j = i + 1; j < no; ++j)
+            if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return true;
+    }
+    return false;
+}
+
+// Hidden-slice plan: slice width = 32 * d with d | H/32, chosen to minimise
+// (waves of kPlanSlots CTAs) x (chunks per CTA + 2 chunks of fixed cost).
+void plan(long long T, int H, int *n_slices, int *slice_w) {
+    const int chunks = H / kChunk;
+    const long long tiles = (T + kTileT - 1) / kTileT;
+    long long best_cost = -1;
+    int best_d = chunks;
+    for (int d = 1; d <= chunks; ++d) {
+        if (chunks % d) continue;
+        const long long ctas = tiles * (chunks / d);
+        const long long waves = (ctas + kPlanSlots - 1) / kPlanSlots;
+        const long long cost = waves * (d + 2);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best_d = d;
+        }
+    }
+    *n_slices = chunks / best_d;
+    *slice_w = best_d * kChunk;
+}
+
+size_t workspace_bytes(long long T, int H) {
+    if (T <= 0 || !hidden_ok(H)) return 0;
+    int S = 0, w = 0;
+    plan(T, H, &S, &w);
+    const size_t b = static_cast<size_t>(S) * static_cast<size_t>(T) * kPartStride * sizeof(float);
+    return (b + 255) & ~static_cast<size_t>(255);
+}
+
+// bf16 [rows.., H] viewed by TMA: dim0 = hidden (box 32, 64-byte swizzle).
+bool encode_2d(CUtensorMap *m, const void *ptr, int H, long long T) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[2] = {kChunk, kTileT};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// bf16 [T, 4, H] viewed as (hidden, token, stream) so that a box lands in
+// shared memory as [stream][token][32 hidden].
+bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T) {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T), 4};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * 8, static_cast<cuuint64_t>(H) * 2};
+    cuuint32_t box[3] = {kChunk, kTileT, 4};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+mhc_status check_params(const mhc_params *p) {
+    if (!p) return MHC_ERR_NULL;
+    if (p->sinkhorn_iters < 1) return MHC_ERR_SHAPE;
+    return MHC_OK;
+}
+
+CoefArgs coef_args(const float *scale, const float *base, const mhc_params *p) {
+    CoefArgs c;
+    c.scale = scale;
+    c.base = base;
+    c.hc_norm_eps = p->hc_norm_eps;
+    c.hc_pre_eps = p->hc_pre_eps;
+    c.hc_post_mult = p->hc_post_mult;
+    c.sinkhorn_eps = p->sinkhorn_eps;
+    c.norm_eps = p->norm_eps;
+    c.sinkhorn_iters = p->sinkhorn_iters;
+    return c;
+}
+
+mhc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
+
+// Shared body of mhc_pre (x == NULL) and mhc_boundary_fused.
+mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, const float *post,
+                        const float *comb, const float *pre_lag, const void *weight,
+                        const float *scale, const float *base, const void *norm_w,
+                        mhc_dtype norm_dtype, const mhc_params *params, long long T, int H,
+                        uint16_t *residual_out, uint16_t *layer_input, float *pre_out,
+                        float *post_out, float *comb_out, void *workspace, size_t ws_bytes,
+                        void *stream) {
+    if (T < 0) return MHC_ERR_SHAPE;
+    if (mhc_status s = check_params(params)) return s;
+    if (!hidden_ok(H)) return MHC_ERR_UNSUPPORTED;
+    if (norm_w && norm_dtype != MHC_F32 && norm_dtype != MHC_BF16) return MHC_ERR_SHAPE;
+    if (T == 0) return MHC_OK;
+    const bool fused = mode != PRE_ONLY;
+    const void *need[] = {residual, weight, scale, base, layer_input, pre_out, post_out, comb_out,
+                          workspace};
+    for (const void *p : need)
+        if (!p) return MHC_ERR_NULL;
+    if (fused && (!x || !post || !comb || !residual_out)) return MHC_ERR_NULL;
+    if (mode == FUSED_SHIFTED && !pre_lag) return MHC_ERR_NULL;
+    const void *al[] = {x, residual, post, comb, pre_lag, weight, scale, base, norm_w,
+                        residual_out, layer_input, pre_out, post_out, comb_out, workspace};
+    for (const void *p : al)
+        if (p && !aligned16(p)) return MHC_ERR_ALIGN;
+    if (ws_bytes < workspace_bytes(T, H)) return MHC_ERR_WORKSPACE;
+
+    const size_t nres = static_cast<size_t>(T) * 4 * H * 2, nx = static_cast<size_t>(T) * H * 2;
+    const size_t n4 = static_cast<size_t>(T) * 16, n16 = static_cast<size_t>(T) * 64;
+    const size_t nw = norm_w ? static_cast<size_t>(H) * (norm_dtype == MHC_BF16 ? 2 : 4) : 0;
+    const Range ins[] = {{x, fused ? nx : 0}, {residual, nres}, {post, fused ? n4 : 0},
+                         {comb, fused ? n16 : 0}, {pre_lag, pre_lag ? n4 : 0},
+                         {weight, mhc_weight_bytes(H)}, {scale, 12}, {base, 96}, {norm_w, nw}};
+    const Range outs[] = {{fused ? residual_out : nullptr, fused ? nres : 0},
+                          {layer_input, nx}, {pre_out, n4}, {post_out, n4}, {comb_out, n16},
+                          {workspace, ws_bytes}};
+    if (aliasing(outs, 6, ins, 9, residual, residual_out)) return MHC_ERR_ALIAS;
+
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    if (!get_encoder()) return MHC_ERR_CUDA;
+
+    int S = 0, w = 0;
+    plan(T, H, &S, &w);
+    CUtensorMap m_res, m_x, m_rout, m_li;
+    if (!encode_res(&m_res, residual, H, T)) return MHC_ERR_CUDA;
+    m_x = m_rout = m_li = m_res;
+    if (fused) {
+        if (!encode_2d(&m_x, x, H, T) || !encode_res(&m_rout, residual_out, H, T))
+            return MHC_ERR_CUDA;
+        if (mode == FUSED_SHIFTED && !encode_2d(&m_li, layer_input, H, T)) return MHC_ERR_CUDA;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    StreamArgs sa;
+    sa.post = post;
+    sa.comb = comb;
+    sa.pre_lag = pre_lag;
+    sa.weight = static_cast<const uint8_t *>(weight);
+    sa.partials = static_cast<float *>(workspace);
+    sa.status = dev->status;
+    sa.T = T;
+    sa.H = H;
+    sa.slice_w = w;
+    sa.timeout_ns = g_timeout_ns.load();
+    const int tiles = static_cast<int>((T + kTileT - 1) / kTileT);
+    if (mhc_status s = cuda_status(launch_stream(mode, kStages, m_res, m_x, m_rout, m_li, sa, S,
+                                                 tiles, st)))
+        return s;
+    if (t_between_event) {
+        cudaEvent_t ev = t_between_event;
+        t_between_event = nullptr;
+        if (cudaEventRecord(ev, st) != cudaSuccess) return MHC_ERR_CUDA;
+    }
+
+    FinishArgs fa;
+    fa.partials = static_cast<const float *>(workspace);
+    fa.n_slices = S;
+    fa.coef = coef_args(scale, base, params);
+    fa.norm_w = norm_w;
+    fa.nw_bf16 = norm_dtype == MHC_BF16;
+    fa.cur = mode == FUSED_UNSHIFTED ? residual_out : residual;
+    fa.layer_input = layer_input;
+    fa.pre_out = pre_out;
+    fa.post_out = post_out;
+    fa.comb_out = comb_out;
+    fa.T = T;
+    fa.H = H;
+    if (mode == FUSED_SHIFTED) return cuda_status(launch_finish_shifted(fa, st));
+    return cuda_status(launch_finish_unshifted(fa, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mhc_weight_bytes(int hidden) {
+    return hidden_ok(hidden) ? static_cast<size_t>(384) * hidden : 0;
+}
+
+size_t mhc_workspace_bytes(int64_t tokens, int hidden) { return workspace_bytes(tokens, hidden); }
+
+mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width) {
+    if (!n_slices || !slice_width) return MHC_ERR_NULL;
+    if (tokens < 0) return MHC_ERR_SHAPE;
+    if (!hidden_ok(hidden)) return MHC_ERR_UNSUPPORTED;
+    plan(tokens, hidden, n_slices, slice_width);
+    return MHC_OK;
+}
+
+mhc_status mhc_prepare_weight(const float *fn, int hidden, void *weight, void *stream) {
+    if (!hidden_ok(hidden)) return MHC_ERR_UNSUPPORTED;
+    if (!fn || !weight) return MHC_ERR_NULL;
+    if (!aligned16(fn) || !aligned16(weight)) return MHC_ERR_ALIGN;
+    if (overlap(fn, static_cast<size_t>(96) * 4 * hidden, weight, mhc_weight_bytes(hidden)))
+        return MHC_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    return cuda_status(launch_prepare_weight(fn, hidden, static_cast<uint8_t *>(weight),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+mhc_status mhc_post(const uint16_t *x, const uint16_t *residual, const float *post,
+                    const float *comb, uint16_t *residual_out, int64_t tokens, int hidden,
+                    void *stream) {
+    if (tokens < 0) return MHC_ERR_SHAPE;
+    if (!hidden_ok(hidden)) return MHC_ERR_UNSUPPORTED;
+    if (tokens == 0) return MHC_OK;
+    if (!x || !residual || !post || !comb || !residual_out) return MHC_ERR_NULL;
+    const void *al[] = {x, residual, post, comb, residual_out};
+    for (const void *p : al)
+        if (!aligned16(p)) return MHC_ERR_ALIGN;
+    const size_t nres = static_cast<size_t>(tokens) * 4 * hidden * 2;
+    const Range ins[] = {{x, static_cast<size_t>(tokens) * hidden * 2}, {residual, nres},
+                         {post, static_cast<size_t>(tokens) * 16},
+                         {comb, static_cast<size_t>(tokens) * 64}};
+    const Range outs[] = {{residual_out, nres}};
+    if (aliasing(outs, 1, ins, 4, residual, residual_out)) return MHC_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    return cuda_status(launch_post(x, residual, post, comb, residual_out, tokens, hidden,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+mhc_status mhc_pre(const uint16_t *residual, const void *weight, const float *scale,
+                   const float *base, const void *norm_w, mhc_dtype norm_dtype,
+                   const mhc_params *params, int64_t tokens, int hidden, uint16_t *layer_input,
+                   float *pre_out, float *post_out, float *comb_out, void *workspace,
+                   size_t workspace_bytes, void *stream) {
+    return run_boundary(PRE_ONLY, nullptr, residual, nullptr, nullptr, nullptr, weight, scale,
+                        base, norm_w, norm_dtype, params, tokens, hidden, nullptr, layer_input,
+                        pre_out, post_out, comb_out, workspace, workspace_bytes, stream);
+}
+
+mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual, const float *post,
+                              const float *comb, const float *pre_lag, const void *weight,
+                              const float *scale, const float *base, const void *norm_w,
+                              mhc_dtype norm_dtype, const mhc_params *params, int64_t tokens,
+                              int hidden, uint16_t *residual_out, uint16_t *layer_input,
+                              float *pre_out, float *post_out, float *comb_out, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+    return run_boundary(pre_lag ? FUSED_SHIFTED : FUSED_UNSHIFTED, x, residual, post, comb,
+                        pre_lag, weight, scale, base, norm_w, norm_dtype, params, tokens, hidden,
+                        residual_out, layer_input, pre_out, post_out, comb_out, workspace,
+                        workspace_bytes, stream);
+}
+
+mhc_status mhc_get_device_status(void *stream) {
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MHC_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MHC_ERR_CUDA;
+    if (word == 0) return MHC_OK;
+    if (cudaMemset(dev->status, 0, sizeof word) != cudaSuccess) return MHC_ERR_CUDA;
+    t_last_site = static_cast<int>(word >> 8);
+    const int code = static_cast<int>(word & 0xFF);
+    return code == MHC_ERR_DEVICE_TIMEOUT ? MHC_ERR_DEVICE_TIMEOUT : MHC_ERR_CUDA;
+}
+
+int mhc_last_timeout_site(void) { return t_last_site; }
+
+const char *mhc_status_string(mhc_status s) {
+    switch (s) {
+        case MHC_OK: return "MHC_OK";
+        case MHC_ERR_NULL: return "MHC_ERR_NULL: a required pointer is NULL";
+        case MHC_ERR_ALIGN: return "MHC_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case MHC_ERR_SHAPE: return "MHC_ERR_SHAPE: bad token count or parameters";
+        case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: hidden size or device not supported";
+        case MHC_ERR_ALIAS: return "MHC_ERR_ALIAS: an output overlaps an input or another output";
+        case MHC_ERR_CUDA: return "MHC_ERR_CUDA: a CUDA call failed";
+        case MHC_ERR_DEVICE_TIMEOUT: return "MHC_ERR_DEVICE_TIMEOUT: a device-side wait ran out";
+        case MHC_ERR_WORKSPACE: return "MHC_ERR_WORKSPACE: workspace missing or too small";
+    }
+    return "unknown mhc_status";
+}
+
+void mhc_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1000000000ull); }
+
+void mhc_debug_record_between(void *event) {
+    t_between_event = static_cast<cudaEvent_t>(event);
+}
+
+mhc_status mhc_debug_unarmed_wait(void *stream) {
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    return cuda_status(
+        launch_unarmed_wait(dev->status, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal declarations shared by the kernel translation units and the host
+// API. Not part of the C ABI.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mhc {
+
+enum Mode : int { PRE_ONLY = 0, FUSED_UNSHIFTED = 1, FUSED_SHIFTED = 2 };
+
+constexpr int kTileT = 128;                         // tokens per CTA tile (MMA M)
+constexpr int kChunk = 32;                          // hidden per pipeline stage
+constexpr int kRowBytes = kChunk * 2;               // one 64-byte bf16 row
+constexpr int kResBytes = 4 * kTileT * kRowBytes;   // residual / cur tile
+constexpr int kXBytes = kTileT * kRowBytes;         // x / collapse tile
+constexpr int kWRows = 48;                          // 24 hi + 24 lo weight rows
+constexpr int kWBytes = 4 * kWRows * kRowBytes;     // weight tile of one chunk
+constexpr int kStageBytes = kResBytes + kXBytes + kWBytes;
+constexpr int kPartStride = 28;                     // floats per token per slice
+constexpr int kStreamThreads = 320;                 // TMA warp, MMA warp, 8 workers
+constexpr int kTmemCols = 64;
+
+struct StreamArgs {
+    const float *post;       // [T,4]
+    const float *comb;       // [T,4,4]
+    const float *pre_lag;    // [T,4] (shifted only)
+    const uint8_t *weight;   // prepared tiles
+    float *partials;         // [n_slices][T][kPartStride]
+    unsigned int *status;    // device status word
+    long long T;
+    int H;
+    int slice_w;             // hidden per slice (multiple of kChunk)
+    unsigned long long timeout_ns;
+};
+
+struct CoefArgs {
+    const float *scale;
+    const float *base;
+    float hc_norm_eps, hc_pre_eps, hc_post_mult, sinkhorn_eps, norm_eps;
+    int sinkhorn_iters;
+};
+
+struct FinishArgs {
+    const float *partials;   // [n_slices][T][kPartStride]
+    int n_slices;
+    CoefArgs coef;
+    const void *norm_w;      // [H] or NULL
+    int nw_bf16;
+    const uint16_t *cur;     // [T,4,H] stream the collapse reads (unshifted)
+    uint16_t *layer_input;   // [T,H]
+    float *pre_out, *post_out, *comb_out;
+    long long T;
+    int H;
+};
+
+size_t stream_smem_bytes(int stages);
+cudaError_t launch_stream(int mode, int stages, const CUtensorMap &res, const CUtensorMap &x,
+                          const CUtensorMap &rout, const CUtensorMap &li,
+                          const StreamArgs &a, int n_slices, int n_tiles, cudaStream_t s);
+cudaError_t launch_finish_shifted(const FinishArgs &a, cudaStream_t s);
+cudaError_t launch_finish_unshifted(const FinishArgs &a, cudaStream_t s);
+cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s);
+cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *post,
+                        const float *comb, uint16_t *out, long long T, int H, cudaStream_t s);
+cudaError_t launch_unarmed_wait(unsigned int *status, unsigned long long timeout_ns,
+                                cudaStream_t s);
+unsigned int *device_status_word();   // of the current device; NULL on failure
+
+}  // namespace mhc

@@ -60,19 +60,43 @@ def make_inputs(T: int, H: int, seed: int, *, residual_std: float = 1.0,
         mask = torch.rand(T, 4, H, generator=g) < outlier_frac
         res = torch.where(mask, res * outlier_mult, res)
     x = torch.randn(T, H, generator=g, dtype=torch.float32)
+    return _finish(g, T, H, res, x, base_std, with_fn)
+
+
+def make_inputs_device(T: int, H: int, seed: int, device, *, residual_std: float = 1.0,
+                       outlier_frac: float = 0.0, outlier_mult: float = 100.0,
+                       base_std: float = 0.1) -> dict:
+    """Same recipe for large workloads: residual and x are drawn on `device`
+    by a generator seeded with `seed` and stay there as bf16 tensors
+    (``residual_dev``, ``x_dev``); the small tensors come from a CPU generator
+    seeded with ``seed + 1`` as numpy arrays. Rows needed on the host are
+    copied back by the caller."""
+    gd = torch.Generator(device).manual_seed(int(seed))
+    res = torch.randn(T, 4, H, generator=gd, dtype=torch.float32, device=device)
+    res.mul_(residual_std)
+    if outlier_frac > 0.0 and res.numel() > 0:
+        mask = torch.rand(T, 4, H, generator=gd, device=device) < outlier_frac
+        res = torch.where(mask, res * outlier_mult, res)
+    x = torch.randn(T, H, generator=gd, dtype=torch.float32, device=device)
+    g = torch.Generator("cpu").manual_seed(int(seed) + 1)
+    out = _finish(g, T, H, None, None, base_std, True)
+    out["residual_dev"] = res.to(torch.bfloat16)
+    del res
+    out["x_dev"] = x.to(torch.bfloat16)
+    return out
+
+
+def _finish(g, T, H, res, x, base_std, with_fn):
     post = torch.rand(T, 4, generator=g, dtype=torch.float32) * 2.0
     # Birkhoff: convex weights from normalised exponential draws
     e = -torch.log(torch.rand(T, 24, generator=g, dtype=torch.float64).clamp_min(1e-300))
     lam = (e / e.sum(dim=1, keepdim=True)).numpy()
     comb = np.einsum("tp,pij->tij", lam, _PERMS).astype(np.float32)
     pre_lag = (torch.rand(T, 4, generator=g, dtype=torch.float32) + 1e-6).numpy()
-    out = dict(
-        residual=_bf16_bits(res),
-        x=_bf16_bits(x),
-        post=post.numpy(),
-        comb=comb,
-        pre_lag=pre_lag,
-    )
+    out = dict(post=post.numpy(), comb=comb, pre_lag=pre_lag)
+    if res is not None:
+        out["residual"] = _bf16_bits(res)
+        out["x"] = _bf16_bits(x)
     if with_fn:
         K = 4 * H
         out["fn"] = (torch.randn(24, K, generator=g, dtype=torch.float32)

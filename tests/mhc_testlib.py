@@ -1,0 +1,136 @@
+"""Helpers shared by the GPU parity tests: moving the seeded inputs to the
+device, running the library through its C ABI, and comparing with the CPU
+oracle at the tolerances stated in the tests."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle as orc
+from manifold_constrained_hyper_gb300 import ops
+
+MODES = {"pre": orc.MODE_PRE_ONLY, "unshifted": orc.MODE_FUSED_UNSHIFTED,
+         "shifted": orc.MODE_FUSED_SHIFTED}
+
+# Tolerances (derivation in DESIGN.md "Parity bar"):
+COEF_RTOL, COEF_ATOL = 1e-5, 1e-7      # pre, post, comb
+MIX_RTOL = 1e-5                         # |g - o| <= 1e-5 * max(|o|, ||terms||_2)
+
+
+def dev_bf16(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def dev_f32(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bf16_ulp_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in bf16 ulps between bit patterns (+0 and -0 coincide)."""
+    def ordered(u):
+        v = u.astype(np.int32)
+        return np.where(v & 0x8000, -(v & 0x7FFF), v)
+    return np.abs(ordered(a) - ordered(b))
+
+
+def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = None,
+            weight=None, in_place: bool = False, dev_tensors: dict | None = None):
+    """Runs one boundary call on the GPU. `d` holds numpy inputs (synth);
+    `dev_tensors` may carry residual/x already on the device. Returns a dict
+    of numpy outputs plus the workspace partials [S][T][28]."""
+    dev_tensors = dev_tensors or {}
+    res = dev_tensors.get("residual")
+    if res is None:
+        res = dev_bf16(d["residual"])
+    T, _, H = res.shape
+    fn = dev_f32(d["fn"])
+    w = weight if weight is not None else ops.mhc_prepare_weight(fn)
+    scale, base = dev_f32(d["scale"]), dev_f32(d["base"])
+    nw = None
+    if norm == "f32":
+        nw = dev_f32(d["norm_w"])
+    elif norm == "bf16":
+        nw = dev_bf16(orc.f32_to_bf16(d["norm_w"]))
+    ws = torch.empty(max(ops.workspace_bytes(T, H), 16), dtype=torch.uint8, device="cuda")
+    out = {}
+    if mode == "pre":
+        li, pr, po, cb = ops.mhc_pre(res, w, scale, base, nw, params, workspace=ws)
+    else:
+        x = dev_tensors.get("x")
+        if x is None:
+            x = dev_bf16(d["x"])
+        pl = dev_f32(d["pre_lag"]) if mode == "shifted" else None
+        rout = res if in_place else None
+        ro, li, pr, po, cb = ops.mhc_boundary_fused(
+            x, res, dev_f32(d["post"]), dev_f32(d["comb"]), w, scale, base, nw, pl, params,
+            residual_out=rout, workspace=ws)
+        out["residual_out_dev"] = ro
+    torch.cuda.synchronize()
+    assert ops.mhc_get_device_status() == 0
+    S, _ = ops.plan(T, H)
+    part = ws[: S * T * 28 * 4].view(torch.float32).view(S, T, 28).cpu().numpy()
+    out.update(layer_input_dev=li, pre=pr.cpu().numpy(), post=po.cpu().numpy(),
+               comb=cb.cpu().numpy(), partials=part)
+    return out
+
+
+def gpu_mixes(partials: np.ndarray) -> np.ndarray:
+    """Sum of the slice partials in slice order, in fp32 (as the finishing
+    kernel does): [T, 24]."""
+    acc = np.zeros(partials.shape[1:], np.float32)
+    for s in range(partials.shape[0]):
+        acc = (acc + partials[s]).astype(np.float32)
+    return acc[:, :24]
+
+
+def run_oracle(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = None,
+               rows=None):
+    p = params or ops.Params()
+    op = orc.OracleParams(p.hc_norm_eps, p.hc_pre_eps, p.hc_post_mult, p.sinkhorn_eps,
+                          p.norm_eps, p.sinkhorn_iters)
+    nw = None
+    if norm == "f32":
+        nw = d["norm_w"]
+    elif norm == "bf16":
+        nw = orc.f32_to_bf16(d["norm_w"])
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    kw = {}
+    if mode != "pre":
+        kw = dict(x=sel(d["x"]), post_mix=sel(d["post"]), comb=sel(d["comb"]))
+        if mode == "shifted":
+            kw["pre_lag"] = sel(d["pre_lag"])
+    return orc.boundary(MODES[mode], sel(d["residual"]), d["fn"], d["scale"], d["base"], nw,
+                        params=op, **kw)
+
+
+def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: bool = True):
+    """Element-wise comparison of GPU outputs (optionally the token `rows`)
+    with the oracle's. Returns a dict of observed error figures."""
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    stats = {}
+    if mode != "pre":
+        ro = sel(host_bits(g["residual_out_dev"]))
+        assert np.array_equal(ro, o["residual_out"]), "residual_out differs"
+    li = sel(host_bits(g["layer_input_dev"]))
+    du = bf16_ulp_diff(li, o["layer_input"])
+    stats["li_max_ulp"] = int(du.max()) if du.size else 0
+    stats["li_frac_exact"] = float(np.mean(du == 0)) if du.size else 1.0
+    assert stats["li_max_ulp"] <= li_ulps, stats
+    for k in ("pre", "post", "comb"):
+        gv, ov = sel(g[k]).astype(np.float64), o[k].astype(np.float64)
+        err = np.abs(gv - ov)
+        bound = COEF_RTOL * np.abs(ov) + COEF_ATOL
+        stats[k + "_max_rel"] = float(np.max(err / np.maximum(np.abs(ov), 1e-30)))
+        assert np.all(err <= bound), (k, float(np.max(err - bound)))
+    if mixes:
+        gm = sel(gpu_mixes(g["partials"])).astype(np.float64)
+        om = o["mix"].astype(np.float64)
+        scale = np.maximum(np.abs(om), o["mix_scale"].astype(np.float64))
+        err = np.abs(gm - om)
+        stats["mix_max_scaled"] = float(np.max(err / scale))
+        assert np.all(err <= MIX_RTOL * scale), stats["mix_max_scaled"]
+    return stats

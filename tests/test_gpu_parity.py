@@ -1,0 +1,231 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs. Bar: bit-exact for the prepared weight and the updated
+residual; layer input within 1 bf16 ulp (shifted, where the collapse is
+exact) or 2 ulps (unshifted, where pre feeds a second bf16 rounding);
+coefficients within 1e-5 relative + 1e-7; mixes within 1e-5 of
+max(|mix|, ||terms||_2)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from manifold_constrained_hyper_gb300 import ops, synth
+from tests.mhc_testlib import (bf16_ulp_diff, compare, dev_bf16, dev_f32, host_bits, run_gpu,
+                               run_oracle)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from manifold_constrained_hyper_gb300 import build
+    build.build()
+    ops.load()
+
+
+# ------------------------------------------------------------------ weight prep
+
+
+@pytest.mark.parametrize("H", [32, 256, 4096, 7168])
+def test_prepare_weight_bit_exact(H):
+    d = synth.make_inputs(1, H, seed=100 + H)
+    w = ops.mhc_prepare_weight(dev_f32(d["fn"]))
+    torch.cuda.synchronize()
+    got = w.cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, orc.weight_tiles(d["fn"], H))
+
+
+def test_prepare_weight_rounding_edge_values():
+    H = 32
+    fn = np.zeros((24, 4 * H), np.float32)
+    special = np.array([0x3F801000, 0xBF801000, 0x3F800FFF, 0x3FFFF000, 0x00000000,
+                        0x80000000, 0x7F7FF000, 0x33FFFFFF], np.uint32).view(np.float32)
+    fn.reshape(-1)[: special.size] = special
+    fn.reshape(-1)[100:100 + 1000] = np.random.default_rng(1).standard_normal(1000)
+    w = ops.mhc_prepare_weight(dev_f32(fn))
+    torch.cuda.synchronize()
+    assert np.array_equal(w.cpu().numpy().view(np.uint16), orc.weight_tiles(fn, H))
+
+
+# ------------------------------------------------------------------ post
+
+
+@pytest.mark.parametrize("T,H", [(1, 256), (3, 7168), (17, 512), (200, 4096)])
+def test_post_bit_exact(T, H):
+    d = synth.make_inputs(T, H, seed=200 + T)
+    out = ops.mhc_post(dev_bf16(d["x"]), dev_bf16(d["residual"]), dev_f32(d["post"]),
+                       dev_f32(d["comb"]))
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(out), orc.post(d["x"], d["residual"], d["post"], d["comb"]))
+
+
+def test_post_in_place_and_subnormals():
+    T, H = 5, 256
+    d = synth.make_inputs(T, H, seed=205)
+    d["residual"][0, 0, :8] = np.array([1, 2, 0x8001, 0x0080, 0x007F, 0x8000, 0, 0x3F80],
+                                       np.uint16)
+    d["post"][1, :] = 2.0 ** -100
+    want = orc.post(d["x"], d["residual"], d["post"], d["comb"])
+    res = dev_bf16(d["residual"])
+    ops.mhc_post(dev_bf16(d["x"]), res, dev_f32(d["post"]), dev_f32(d["comb"]), out=res)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(res), want)
+
+
+# ------------------------------------------------------------------ boundary
+
+
+def test_tiny_t4_h256_all_modes():
+    d = synth.workload_inputs("tiny_t4_h256")
+    for mode in ("shifted", "unshifted", "pre"):
+        g = run_gpu(mode, d)
+        o = run_oracle(mode, d)
+        compare(mode, g, o, li_ulps=1 if mode == "shifted" else 2)
+
+
+@pytest.mark.parametrize("T", synth.DECODE_TOKENS)
+def test_decode_sweep_shifted_h7168(T):
+    d = synth.make_inputs(**synth.decode_workload(T))
+    g = run_gpu("shifted", d)
+    o = run_oracle("shifted", d)
+    compare("shifted", g, o, li_ulps=1)
+
+
+@pytest.mark.parametrize("mode", ["shifted", "unshifted", "pre"])
+@pytest.mark.parametrize("T,H", [(129, 256), (200, 512), (333, 1024), (130, 4096)])
+def test_ragged_tiles(mode, T, H):
+    d = synth.make_inputs(T, H, seed=300 + T + H)
+    g = run_gpu(mode, d)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, li_ulps=1 if mode == "shifted" else 2)
+
+
+@pytest.mark.parametrize("mode", ["pre", "unshifted", "shifted"])
+def test_mid_batch_t512_h7168(mode):
+    d = synth.workload_inputs("mid_t512_h7168")
+    g = run_gpu(mode, d)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, li_ulps=1 if mode == "shifted" else 2)
+
+
+@pytest.mark.parametrize("norm", ["bf16", None])
+def test_norm_weight_variants(norm):
+    d = synth.make_inputs(40, 512, seed=401)
+    for mode in ("shifted", "unshifted", "pre"):
+        g = run_gpu(mode, d, norm=norm)
+        o = run_oracle(mode, d, norm=norm)
+        compare(mode, g, o, li_ulps=1 if mode == "shifted" else 2)
+
+
+def test_in_place_residual():
+    d = synth.make_inputs(70, 1024, seed=402)
+    o = run_oracle("shifted", d)
+    g = run_gpu("shifted", d, in_place=True)
+    compare("shifted", g, o)
+
+
+def test_zero_tokens_is_a_noop():
+    w = ops.mhc_prepare_weight(torch.zeros(24, 4 * 256, device="cuda"))
+    e = torch.empty(0, 4, 256, dtype=torch.bfloat16, device="cuda")
+    ro, li, pr, po, cb = ops.mhc_boundary_fused(
+        torch.empty(0, 256, dtype=torch.bfloat16, device="cuda"), e,
+        torch.empty(0, 4, device="cuda"), torch.empty(0, 4, 4, device="cuda"), w,
+        torch.ones(3, device="cuda"), torch.zeros(24, device="cuda"))
+    torch.cuda.synchronize()
+    assert ro.numel() == 0 and li.numel() == 0
+
+
+def test_outputs_stay_inside_their_buffers():
+    """Outputs written into the middle of guarded buffers: the guard bytes
+    around them keep their canary pattern."""
+    T, H = 131, 256
+    d = synth.make_inputs(T, H, seed=403)
+    G = 4096                                   # guard elements each side
+    canary16 = 0x5A5A
+    big_res = torch.full((G * 2 + T * 4 * H,), canary16, dtype=torch.int16, device="cuda")
+    big_li = torch.full((G * 2 + T * H,), canary16, dtype=torch.int16, device="cuda")
+    big_f = torch.full((3, G * 2 + T * 16), 12345.0, device="cuda")
+    rout = big_res[G:G + T * 4 * H].view(torch.bfloat16).view(T, 4, H)
+    li = big_li[G:G + T * H].view(torch.bfloat16).view(T, H)
+    pre = big_f[0, G:G + T * 4].view(T, 4)
+    post = big_f[1, G:G + T * 4].view(T, 4)
+    comb = big_f[2, G:G + T * 16].view(T, 4, 4)
+    w = ops.mhc_prepare_weight(dev_f32(d["fn"]))
+    ops.mhc_boundary_fused(dev_bf16(d["x"]), dev_bf16(d["residual"]), dev_f32(d["post"]),
+                           dev_f32(d["comb"]), w, dev_f32(d["scale"]), dev_f32(d["base"]),
+                           dev_f32(d["norm_w"]), dev_f32(d["pre_lag"]), residual_out=rout,
+                           layer_input=li, pre_out=pre, post_out=post, comb_out=comb)
+    torch.cuda.synchronize()
+    for big, n in ((big_res, T * 4 * H), (big_li, T * H)):
+        assert torch.all(big[:G] == canary16) and torch.all(big[G + n:] == canary16)
+    for i, n in enumerate((T * 4, T * 4, T * 16)):
+        assert torch.all(big_f[i, :G] == 12345.0) and torch.all(big_f[i, G + n:] == 12345.0)
+    o = run_oracle("shifted", d)
+    assert np.array_equal(host_bits(rout), o["residual_out"])
+    assert bf16_ulp_diff(host_bits(li), o["layer_input"]).max() <= 1
+
+
+# ------------------------------------------------------------------ stress
+
+
+@pytest.mark.parametrize("iters", [1, 5, 20])
+def test_stress_t1024_h4096_sampled_and_deterministic(iters):
+    d = synth.workload_inputs("stress_t1024_h4096")
+    p = ops.Params(sinkhorn_iters=iters)
+    rows = np.unique(np.concatenate([[0, 127, 128, 511, 1023],
+                                     np.random.default_rng(iters).integers(0, 1024, 27)]))
+    w = ops.mhc_prepare_weight(dev_f32(d["fn"]))
+    runs = [run_gpu("shifted", d, params=p, weight=w) for _ in range(10)]
+    ref = runs[0]
+    for r in runs[1:]:
+        assert torch.equal(r["residual_out_dev"], ref["residual_out_dev"])
+        assert torch.equal(r["layer_input_dev"], ref["layer_input_dev"])
+        for k in ("pre", "post", "comb"):
+            assert np.array_equal(r[k].view(np.uint32), ref[k].view(np.uint32)), k
+    o = run_oracle("shifted", d, params=p, rows=rows)
+    compare("shifted", ref, o, rows=rows)
+    # unshifted on the same stress inputs
+    g = run_gpu("unshifted", d, params=p, weight=w)
+    o = run_oracle("unshifted", d, params=p, rows=rows)
+    compare("unshifted", g, o, rows=rows, li_ulps=2)
+
+
+# ------------------------------------------------------------------ full size
+
+
+def test_prefill_t8192_h7168_sampled_tokens():
+    """The benchmark's workload and launch configuration, checked on sampled
+    tokens (first/last of tiles, the tail, random) against the oracle."""
+    cfg = synth.WORKLOADS["prefill_t8192_h7168"]
+    T, H = cfg["T"], cfg["H"]
+    d = synth.make_inputs_device(T, H, cfg["seed"], "cuda")
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 4095, 4096, T - 2, T - 1],
+                                     np.random.default_rng(8192).integers(0, T, 40)]))
+    idx = torch.from_numpy(rows).cuda()
+    d["residual"] = host_bits(d["residual_dev"][idx])
+    d["x"] = host_bits(d["x_dev"][idx])
+    g = run_gpu("shifted", d, dev_tensors={"residual": d["residual_dev"], "x": d["x_dev"]})
+    sub = dict(d, post=d["post"][rows], comb=d["comb"][rows], pre_lag=d["pre_lag"][rows])
+    o = run_oracle("shifted", sub)
+    gsel = {k: (v[idx] if isinstance(v, torch.Tensor) else v) for k, v in g.items()
+            if k not in ("partials",)}
+    for k in ("pre", "post", "comb"):
+        gsel[k] = g[k][rows]
+    gsel["partials"] = g["partials"][:, rows]
+    compare("shifted", gsel, o)
+
+
+# ------------------------------------------------------------------ bounded waits
+
+
+def test_unarmed_wait_times_out_and_context_survives():
+    ops.mhc_set_wait_timeout_ns(20_000_000)          # 20 ms
+    try:
+        ops.mhc_debug_unarmed_wait()
+        assert ops.mhc_get_device_status() == 7
+        assert ops.mhc_last_timeout_site() == 99
+        assert ops.mhc_get_device_status() == 0       # read clears the word
+    finally:
+        ops.mhc_set_wait_timeout_ns(0)
+    d = synth.make_inputs(4, 256, seed=404)
+    compare("shifted", run_gpu("shifted", d), run_oracle("shifted", d))
