@@ -229,6 +229,10 @@ def run_ours(args):
     ev_m = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # torch creates CUDA events lazily: record each once so that the handle
+    # handed to the library exists (and no creation lands in the timed region)
+    for e in ev_s + ev_m + ev_e + [t_begin, t_end]:
+        e.record()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()

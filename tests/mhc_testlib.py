@@ -107,9 +107,35 @@ def run_oracle(mode: str, d: dict, norm: str = "f32", params: ops.Params | None 
                         params=op, **kw)
 
 
-def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: bool = True):
+def oracle_layer_input_given_pre(mode: str, d: dict, pre: np.ndarray, norm="f32",
+                                 params=None, rows=None):
+    """The oracle's layer input when the collapse uses the given `pre` [T, 4]
+    (the GPU's own, for the unshifted forms): the unshifted boundary equals
+    the shifted one fed its own pre, and pre-only equals the shifted one with
+    an identity update (x = 0, post = 0, comb = I; a bitwise copy of normal
+    bf16 values)."""
+    dd = dict(d)
+    dd["pre_lag"] = np.ascontiguousarray(pre, np.float32)
+    if mode == "pre":
+        T = d["residual"].shape[0]
+        dd["x"] = np.zeros(d["residual"].shape[::2], np.uint16)
+        dd["post"] = np.zeros((T, 4), np.float32)
+        dd["comb"] = np.broadcast_to(np.eye(4, dtype=np.float32), (T, 4, 4)).copy()
+    return run_oracle("shifted", dd, norm, params, rows)["layer_input"]
+
+
+def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: bool = True,
+            d: dict | None = None, norm="f32", params=None):
     """Element-wise comparison of GPU outputs (optionally the token `rows`)
-    with the oracle's. Returns a dict of observed error figures."""
+    with the oracle's. Returns a dict of observed error figures.
+
+    Layer input: shifted, the collapse is exact on both sides and the bar is
+    1 bf16 ulp against the oracle. Unshifted / pre-only, the collapse uses
+    this boundary's pre, which the two sides form in different summation
+    orders (checked separately at 1e-5); where sum_j pre_j r_j cancels, that
+    difference is amplified without bound in ulps, so the bar is 1 ulp
+    against the oracle's layer input computed from the GPU's own pre, and at
+    least 99.9 % of elements within 1 ulp of the independent oracle."""
     sel = (lambda a: a) if rows is None else (lambda a: a[rows])
     stats = {}
     if mode != "pre":
@@ -119,7 +145,15 @@ def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: boo
     du = bf16_ulp_diff(li, o["layer_input"])
     stats["li_max_ulp"] = int(du.max()) if du.size else 0
     stats["li_frac_exact"] = float(np.mean(du == 0)) if du.size else 1.0
-    assert stats["li_max_ulp"] <= li_ulps, stats
+    if mode == "shifted":
+        assert stats["li_max_ulp"] <= li_ulps, stats
+    else:
+        assert d is not None, "unshifted comparison needs the inputs"
+        assert float(np.mean(du <= 1)) >= 0.999, stats
+        ref = oracle_layer_input_given_pre(mode, d, g["pre"], norm, params, rows)
+        dc = bf16_ulp_diff(li, ref)
+        stats["li_max_ulp_given_pre"] = int(dc.max()) if dc.size else 0
+        assert stats["li_max_ulp_given_pre"] <= 1, stats
     for k in ("pre", "post", "comb"):
         gv, ov = sel(g[k]).astype(np.float64), o[k].astype(np.float64)
         err = np.abs(gv - ov)
