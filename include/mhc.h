@@ -167,6 +167,42 @@ mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* Allocation-free variant. The pages this library follows have no          */
+/* counterpart of this entry point.                                         */
+
+/*
+ * mhc_boundary_fused without a workspace, for callers that cannot allocate
+ * device memory: code running where cudaMalloc is not permitted or not
+ * wanted, such as a serving engine whose memory planner owns every device
+ * allocation, or a latency-critical loop that cannot afford the implicit
+ * device synchronisation of cudaMalloc/cudaFree. Arguments and results are
+ * those of mhc_boundary_fused.
+ *
+ * Scratch: a fixed 4 MiB array in the library's own device memory, which
+ * every GPU that loads the library keeps until the process exits. A call
+ * whose mhc_workspace_bytes(tokens, hidden) exceeds 4 MiB returns
+ * MHC_ERR_WORKSPACE without enqueuing anything (at hidden 7168 this admits
+ * up to 2048 tokens; at hidden 4096 or less, up to 8192).
+ * Set-up: the first call on a device, with that device current, looks up
+ * the array's device address; make that first call before any stream
+ * capture. Sharing: every call on a device uses the same array and leaves
+ * its contents behind; calls that can overlap on the GPU (unordered streams,
+ * concurrent host threads) race on it and must be serialised by the caller.
+ * No entry needs to start at zero: each call writes every entry it reads.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).
+ */
+mhc_status mhc_boundary_fused_noalloc(const uint16_t *x, const uint16_t *residual,
+                                      const float *post, const float *comb,
+                                      const float *pre_lag, const void *weight,
+                                      const float *scale, const float *base,
+                                      const void *norm_w, mhc_dtype norm_dtype,
+                                      const mhc_params *params, int64_t tokens, int hidden,
+                                      uint16_t *residual_out, uint16_t *layer_input,
+                                      float *pre_out, float *post_out, float *comb_out,
+                                      void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* Status and diagnostics.                                                  */
 
 /* Synchronises `stream`, then reads and clears the current device's status

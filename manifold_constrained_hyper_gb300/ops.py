@@ -26,7 +26,7 @@ STATUS_NAMES = {0: "MHC_OK", 1: "MHC_ERR_NULL", 2: "MHC_ERR_ALIGN", 3: "MHC_ERR_
 EXPORTS = ("mhc_weight_bytes", "mhc_prepare_weight", "mhc_post", "mhc_workspace_bytes",
            "mhc_pre", "mhc_boundary_fused", "mhc_get_device_status", "mhc_last_timeout_site",
            "mhc_status_string", "mhc_set_wait_timeout_ns", "mhc_debug_unarmed_wait",
-           "mhc_plan", "mhc_debug_record_between")
+           "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc")
 
 
 class MhcError(RuntimeError):
@@ -78,6 +78,8 @@ def load():
         "mhc_pre": (i32, [P, P, P, P, P, i32, PP, i64, i32, P, P, P, P, P, sz, P]),
         "mhc_boundary_fused": (i32, [P, P, P, P, P, P, P, P, P, i32, PP, i64, i32,
                                      P, P, P, P, P, P, sz, P]),
+        "mhc_boundary_fused_noalloc": (i32, [P, P, P, P, P, P, P, P, P, i32, PP, i64, i32,
+                                             P, P, P, P, P, P]),
         "mhc_get_device_status": (i32, [P]),
         "mhc_last_timeout_site": (i32, []),
         "mhc_status_string": (ctypes.c_char_p, [i32]),
@@ -214,6 +216,35 @@ def mhc_boundary_fused(x, residual, post, comb, weight, scale, base, norm_w=None
         _p(x), _p(residual), _p(post), _p(comb), _p(pre_lag), _p(weight), _p(scale), _p(base),
         _p(nw), nwt, ctypes.byref(p), T, H, _p(residual_out), _p(li), _p(pr), _p(po), _p(cb),
         _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "mhc_boundary_fused")
+    return residual_out, li, pr, po, cb
+
+
+def mhc_boundary_fused_noalloc(x, residual, post, comb, weight, scale, base, norm_w=None,
+                               pre_lag=None, params: Params | None = None, *,
+                               residual_out=None, layer_input=None, pre_out=None,
+                               post_out=None, comb_out=None, stream=None):
+    """mhc_boundary_fused whose scratch is the library's fixed device array
+    (for callers that cannot allocate device memory). Outputs not given are
+    allocated here with torch; pass them all to allocate nothing."""
+    _bf16(x, "x"), _bf16(residual, "residual"), _f32(post, "post"), _f32(comb, "comb")
+    if pre_lag is not None:
+        _f32(pre_lag, "pre_lag")
+    T, n, H = residual.shape
+    params = params or Params()
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    dev = residual.device
+    li = layer_input if layer_input is not None else torch.empty(T, H, dtype=torch.bfloat16,
+                                                                 device=dev)
+    pr = pre_out if pre_out is not None else torch.empty(T, 4, device=dev)
+    po = post_out if post_out is not None else torch.empty(T, 4, device=dev)
+    cb = comb_out if comb_out is not None else torch.empty(T, 4, 4, device=dev)
+    nw, nwt = _nw(norm_w)
+    p = params.c()
+    _check(load().mhc_boundary_fused_noalloc(
+        _p(x), _p(residual), _p(post), _p(comb), _p(pre_lag), _p(weight), _p(scale), _p(base),
+        _p(nw), nwt, ctypes.byref(p), T, H, _p(residual_out), _p(li), _p(pr), _p(po), _p(cb),
+        _stream(stream)), "mhc_boundary_fused_noalloc")
     return residual_out, li, pr, po, cb
 
 
