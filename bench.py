@@ -194,7 +194,9 @@ def run_ours(args):
         dist.barrier()
     ops.load()
     dev = torch.device("cuda", local)
-    cfg = synth.WORKLOADS[args.workload]
+    cfg = dict(synth.WORKLOADS[args.workload])
+    if args.tokens:
+        cfg["T"] = args.tokens
     T, H = cfg["T"], cfg["H"]
     extra = {k: v for k, v in cfg.items() if k not in ("T", "H", "seed")}
     d = synth.make_inputs_device(T, H, cfg["seed"] + 7919 * rank, dev, **extra)
@@ -355,6 +357,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-tokens", type=int, default=256)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (profiling a smaller case)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

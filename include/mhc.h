@@ -181,8 +181,8 @@ mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
  * Scratch: a fixed 4 MiB array in the library's own device memory, which
  * every GPU that loads the library keeps until the process exits. A call
  * whose mhc_workspace_bytes(tokens, hidden) exceeds 4 MiB returns
- * MHC_ERR_WORKSPACE without enqueuing anything (at hidden 7168 this admits
- * up to 2048 tokens; at hidden 4096 or less, up to 8192).
+ * MHC_ERR_WORKSPACE without enqueuing anything (every decode batch of up to
+ * 128 tokens at hidden up to 8192 fits).
  * Set-up: the first call on a device, with that device current, looks up
  * the array's device address; make that first call before any stream
  * capture. Sharing: every call on a device uses the same array and leaves

@@ -15,8 +15,6 @@ using namespace mhc;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kPlanSlots = 2 * 152;   // co-resident stream CTAs on a 152-SM GB300
-constexpr int kStages = 2;
 
 std::atomic<unsigned long long> g_timeout_ns{1000000000ull};
 thread_local int t_last_site = 0;
@@ -95,19 +93,21 @@ bool aliasing(const Range *outs, int no, const Range *ins, int ni, const void *m
     return false;
 }
 
-// Hidden-slice plan: slice width = 32 * d with d | H/32, chosen to minimise
-// (waves of kPlanSlots CTAs) x (chunks per CTA + 2 chunks of fixed cost).
+// Hidden-slice plan: items of d chunks (slice width 32 * d, d | H/32) spread
+// over kGridCap persistent CTAs; minimise the busiest CTA's work, counting an
+// item's partials (written and read back, ~0.35 of a chunk's bytes) as cost.
+// A pure function of (T, H), so the workspace size is too.
 void plan(long long T, int H, int *n_slices, int *slice_w) {
     const int chunks = H / kChunk;
     const long long tiles = (T + kTileT - 1) / kTileT;
-    long long best_cost = -1;
+    double best_cost = -1.0;
     int best_d = chunks;
-    for (int d = 1; d <= chunks; ++d) {
+    for (int d = chunks; d >= 1; --d) {
         if (chunks % d) continue;
-        const long long ctas = tiles * (chunks / d);
-        const long long waves = (ctas + kPlanSlots - 1) / kPlanSlots;
-        const long long cost = waves * (d + 2);
-        if (best_cost < 0 || cost < best_cost) {
+        const long long items = tiles * (chunks / d);
+        const long long per_cta = (items + kGridCap - 1) / kGridCap;
+        const double cost = static_cast<double>(per_cta) * (d + 0.35);
+        if (best_cost < 0 || cost < best_cost - 1e-9) {
             best_cost = cost;
             best_d = d;
         }
@@ -132,7 +132,7 @@ bool encode_2d(CUtensorMap *m, const void *ptr, int H, long long T) {
     cuuint32_t estr[2] = {1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -145,7 +145,7 @@ bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T) {
     cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -233,9 +233,12 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.H = H;
     sa.slice_w = w;
     sa.timeout_ns = g_timeout_ns.load();
-    const int tiles = static_cast<int>((T + kTileT - 1) / kTileT);
-    if (mhc_status s = cuda_status(launch_stream(mode, kStages, m_res, m_x, m_rout, m_li, sa, S,
-                                                 tiles, st)))
+    const long long tiles = (T + kTileT - 1) / kTileT;
+    const long long items = tiles * S;
+    if (items > 0x7FFFFFFFLL) return MHC_ERR_UNSUPPORTED;
+    const int grid = static_cast<int>(items < kGridCap ? items : kGridCap);
+    if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, m_li, sa, S,
+                                                 static_cast<int>(items), grid, st)))
         return s;
     if (t_between_event) {
         cudaEvent_t ev = t_between_event;

@@ -55,10 +55,14 @@ struct FinishArgs {
     int H;
 };
 
-size_t stream_smem_bytes(int stages);
-cudaError_t launch_stream(int mode, int stages, const CUtensorMap &res, const CUtensorMap &x,
-                          const CUtensorMap &rout, const CUtensorMap &li,
-                          const StreamArgs &a, int n_slices, int n_tiles, cudaStream_t s);
+constexpr int kGridCap = 152;                       // persistent CTAs: one per GB300 SM
+
+size_t stream_smem_bytes();
+// Persistent streaming kernel over n_items = tiles x n_slices work items
+// (item i = tile i / n_slices, slice i % n_slices), `grid` CTAs.
+cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x,
+                          const CUtensorMap &rout, const CUtensorMap &li, const StreamArgs &a,
+                          int n_slices, int n_items, int grid, cudaStream_t s);
 cudaError_t launch_finish_shifted(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_finish_unshifted(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s);

@@ -135,6 +135,10 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// All but the most recent bulk group have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_allbut1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
@@ -239,6 +243,23 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 }
 
 // ---------------------------------------------------------------- plain memory
+// 32 contiguous bytes (one L2 sector) to global memory with an L2 policy;
+// `p` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint4 &a, const uint4 &b,
+                                             uint64_t policy) {
+    asm volatile(
+        "st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+        ::"l"(reinterpret_cast<uint64_t>(p)), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x),
+          "r"(b.y), "r"(b.z), "r"(b.w), "l"(policy)
+        : "memory");
+}
+// 16 bytes to global memory with an L2 policy; `p` 16-byte aligned.
+__device__ __forceinline__ void st_global_v4(void *p, const uint4 &a, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+                 ::"l"(reinterpret_cast<uint64_t>(p)), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w),
+                   "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -1,34 +1,43 @@
-// Streaming pass of the mHC boundary: one CTA per (hidden slice, 128-token
-// tile). Per 32-wide hidden chunk of its slice the CTA
-//   1. TMA-loads the residual tile [4 streams][128 tokens][32] and the x tile
-//      [128][32] (bf16, 64-byte swizzled rows) and the chunk's prepared
-//      weight tile [4][48][32] (bulk copy, already in swizzled order);
-//   2. updates the residual in shared memory (post: the flush-to-zero FMA
-//      chain of the "mhc_boundary" page's residual_update), folds the squares
+// Streaming pass of the mHC boundary, persistent: one CTA per SM walks a
+// static list of work items (a 128-token tile x a hidden slice) and runs one
+// continuous chunk pipeline across them. Per 32-wide hidden chunk:
+//   1. TMA-load the residual tile [4 streams][128 tokens][32] and the x tile
+//      [128][32] (bf16, 64-byte swizzled rows) and bulk-load the chunk's
+//      prepared weight tile [4][48][32] (already in swizzled order);
+//   2. workers update the residual in shared memory (post: the flush-to-zero
+//      FMA chain of the "mhc_boundary" page's residual_update), fold squares
 //      of the updated values into per-token sums, and for the shifted form
-//      writes the collapse with the lagged pre (lagged_collapse) over x;
-//   3. TMA-stores the updated residual (and the unnormalised collapse);
-//   4. issues 8 tcgen05 MMAs (M=128 tokens, N=48 stacked hi/lo weight rows,
-//      K=16) accumulating the mixer contraction in TMEM.
-// At the end each token's 24 partial mixes (hi + lo) and its partial sums of
-// squares go to the workspace; a finishing kernel reduces the slices in a
-// fixed order. Warp roles: warp 0 TMA producer and TMEM owner, warp 1 MMA
-// issuer, warps 2-9 elementwise workers (token = 32*(warp%4) + lane, so that
-// a worker reads the TMEM lanes of its own tokens).
+//      write the collapse with the lagged pre (lagged_collapse) over x;
+//   3. TMA-store the updated residual (and the unnormalised collapse);
+//   4. one thread issues 8 tcgen05 MMAs (M=128 tokens, N=48 stacked hi/lo
+//      weight rows, K=16) accumulating the mixer contraction in TMEM.
+// Each item accumulates into one of two TMEM buffers; its epilogue (24
+// partial mixes hi + lo and the partial sums of squares per token, written
+// to the workspace) runs in the workers after they have handled the first
+// chunk of the next item, so neither the MMA nor the stream drains between
+// items. A finishing kernel reduces the slices in a fixed order.
+// Warp roles: warp 0 TMA producer and TMEM owner, warp 1 MMA issuer, warps
+// 2-9 workers (token = 32*(warp%4) + lane: a worker reads the TMEM lanes of
+// its own tokens; warps 2-5 and 6-9 each take two of the four 8-wide units).
 #include "mhc_internal.h"
 #include "ptx.cuh"
 
 namespace mhc {
 namespace {
 
-constexpr int kBarOff(int stages) { return stages * kStageBytes; }
-constexpr int kSsqOff(int stages) { return kBarOff(stages) + 256; }
-constexpr int kMiscOff(int stages) { return kSsqOff(stages) + 2 * kTileT * 4; }
-constexpr int kSmemUsed(int stages) { return kMiscOff(stages) + 64; }
+constexpr int kStages = 4;
+constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kNumBars = 3 * kStages + 8;
+constexpr int kSsqOff = kBarOff + 256;                 // [2 buffers][2 sums][128] fp32
+constexpr int kMiscOff = kSsqOff + 2 * 2 * kTileT * 4;
+constexpr int kSmemUsed = kMiscOff + 64;
+constexpr int kAccCols = 64;                           // one accumulator buffer (48 used)
+static_assert(kNumBars * 8 <= 256, "barrier area");
 
 // Wait-site ids recorded with a timeout.
 enum : int { SITE_PROD_READY = 1, SITE_PROD_MMA = 2, SITE_MMA_FULL = 3, SITE_MMA_READY = 4,
-             SITE_WORK_FULL = 5, SITE_EPI_MMA = 6, SITE_DRAIN = 7 };
+             SITE_WORK_FULL = 5, SITE_EPI_ACC = 6, SITE_DRAIN = 7, SITE_MMA_ACC = 8,
+             SITE_EPI_SSQ = 9, SITE_EPI_SSQ_FREE = 10 };
 
 struct Coefs {
     uint64_t post2[4];       // (post[s], post[s])
@@ -85,54 +94,67 @@ __device__ __forceinline__ uint4 collapse8(const uint4 (&cur)[4], const Coefs &c
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Bounded wait that ignores the abort flag (used to drain copies in flight
-// before the CTA exits after an abort).
+// Bounded wait that ignores the abort flag (drains copies in flight before
+// the CTA exits after an abort).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                            unsigned int *status) {
     int local = 0;
     mbar_wait(bar, parity, &local, timeout_ns, status, SITE_DRAIN);
 }
 
-template <int MODE, int STAGES>
+// Work item k of this CTA -> (tile, slice).
+struct Item {
+    int tile, slice;
+};
+__device__ __forceinline__ Item item_of(int k, int n_slices) {
+    const int i = blockIdx.x + k * gridDim.x;
+    return {i / n_slices, i % n_slices};
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(kStreamThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_rout, const __grid_constant__ CUtensorMap tm_li,
-              const StreamArgs a) {
+              const StreamArgs a, int n_slices, int n_items) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    const uint32_t bars = base + kBarOff(STAGES);
+    const uint32_t bars = base + kBarOff;
     auto full = [&](int st) { return bars + 8u * st; };
-    auto ready = [&](int st) { return bars + 8u * (STAGES + st); };
-    auto mma_done = [&](int st) { return bars + 8u * (2 * STAGES + st); };
-    float *ssq_x = reinterpret_cast<float *>(gbase + kSsqOff(STAGES));
-    float *ssql_x = ssq_x + kTileT;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kMiscOff(STAGES));
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kMiscOff(STAGES) + 16);
+    auto ready = [&](int st) { return bars + 8u * (kStages + st); };
+    auto mma_done = [&](int st) { return bars + 8u * (2 * kStages + st); };
+    auto acc_full = [&](int b) { return bars + 8u * (3 * kStages + b); };
+    auto acc_empty = [&](int b) { return bars + 8u * (3 * kStages + 2 + b); };
+    auto ssq_full = [&](int b) { return bars + 8u * (3 * kStages + 4 + b); };
+    auto ssq_empty = [&](int b) { return bars + 8u * (3 * kStages + 6 + b); };
+    float *ssq_x = reinterpret_cast<float *>(gbase + kSsqOff);   // [b][0: ssq, 1: ssql][t]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kMiscOff);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kMiscOff + 16);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slice = blockIdx.x;
-    const int h0 = slice * a.slice_w;
-    const long long t0 = static_cast<long long>(blockIdx.y) * kTileT;
-    const int n = a.slice_w / kChunk;
+    const int d = a.slice_w / kChunk;                               // chunks per item
+    const int n_local = (n_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
+    const int total = n_local * d;                                   // chunks of this CTA
     const uint64_t tmo = a.timeout_ns;
 
     if (tid == 0) {
-        for (int i = 0; i < STAGES; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(full(i), 1);
             mbar_init(ready(i), 8);
             mbar_init(mma_done(i), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full(b), 1);
+            mbar_init(acc_empty(b), 4);
+            mbar_init(ssq_full(b), 4);
+            mbar_init(ssq_empty(b), 4);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_alloc(smem_addr(tmem_slot), 2 * kAccCols);
         tmem_relinquish();
     }
     if (tid == 32) {
@@ -143,56 +165,61 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_d = *tmem_slot;
+    const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
             const uint64_t pol_stream = policy_evict_first();
-            const uint64_t pol_w = policy_evict_last();
+            const uint64_t pol_keep = policy_evict_last();
             constexpr uint32_t kLoadBytes =
                 kResBytes + kWBytes + (MODE != PRE_ONLY ? kXBytes : 0);
-            auto issue_load = [&](int c) {
-                const int st = c % STAGES;
+            auto issue_load = [&](int g) {
+                const int st = g % kStages;
                 const uint32_t sb = base + st * kStageBytes;
-                const int hc = h0 + c * kChunk;
+                const Item it = item_of(g / d, n_slices);
+                const int hc = it.slice * a.slice_w + (g % d) * kChunk;
+                const int t0 = it.tile * kTileT;
                 mbar_arrive_expect_tx(full(st), kLoadBytes);
-                tma_load_3d(sb, &tm_res, hc, static_cast<int>(t0), 0, full(st), pol_stream);
-                if (MODE != PRE_ONLY)
-                    tma_load_2d(sb + kResBytes, &tm_x, hc, static_cast<int>(t0), full(st),
-                                pol_stream);
+                tma_load_3d(sb, &tm_res, hc, t0, 0, full(st), pol_stream);
+                if (MODE != PRE_ONLY) tma_load_2d(sb + kResBytes, &tm_x, hc, t0, full(st), pol_stream);
                 bulk_load(sb + kResBytes + kXBytes,
                           a.weight + static_cast<size_t>(hc / kChunk) * kWBytes, kWBytes,
-                          full(st), pol_w);
+                          full(st), pol_keep);
             };
             int loaded = 0;
-            for (; loaded < n && loaded < STAGES; ++loaded) issue_load(loaded);
-            int j = 0;
-            for (; j < n; ++j) {
-                const int st = j % STAGES;
-                const uint32_t ph = (j / STAGES) & 1;
+            for (; loaded < total && loaded < kStages; ++loaded) issue_load(loaded);
+            int g = 0;
+            for (; g < total; ++g) {
+                const int st = g % kStages;
+                const uint32_t ph = (g / kStages) & 1;
                 if (!mbar_wait(ready(st), ph, abort_flag, tmo, a.status, SITE_PROD_READY)) break;
-                const uint32_t sb = base + st * kStageBytes;
                 if (MODE != PRE_ONLY) {
-                    tma_store_3d(&tm_rout, h0 + j * kChunk, static_cast<int>(t0), 0, sb,
-                                 pol_stream);
-                    if (MODE == FUSED_SHIFTED)
-                        tma_store_2d(&tm_li, h0 + j * kChunk, static_cast<int>(t0),
-                                     sb + kResBytes, pol_stream);
+                    const uint32_t sb = base + st * kStageBytes;
+                    const Item it = item_of(g / d, n_slices);
+                    const int hc = it.slice * a.slice_w + (g % d) * kChunk;
+                    const int t0 = it.tile * kTileT;
+                    tma_store_3d(&tm_rout, hc, t0, 0, sb, pol_stream);
+                    // the collapse is re-read by the finishing kernel: keep it in L2
+                    if (MODE == FUSED_SHIFTED) tma_store_2d(&tm_li, hc, t0, sb + kResBytes, pol_keep);
                     bulk_commit();
                 }
-                if (loaded < n) {
-                    if (MODE != PRE_ONLY) bulk_wait_read_all();
-                    if (!mbar_wait(mma_done(st), ph, abort_flag, tmo, a.status, SITE_PROD_MMA))
+                // refill the stage of the previous chunk: its stores have had a
+                // whole chunk to read shared memory
+                if (g >= 1 && loaded < total) {
+                    const int gp = g - 1;
+                    if (MODE != PRE_ONLY) bulk_wait_read_allbut1();
+                    if (!mbar_wait(mma_done(gp % kStages), (gp / kStages) & 1, abort_flag, tmo,
+                                   a.status, SITE_PROD_MMA))
                         break;
                     issue_load(loaded);
                     ++loaded;
                 }
             }
             bulk_wait_all();
-            if (j < n) {  // aborted: let the loads in flight land before exiting
-                for (int c = j; c < loaded; ++c)
-                    drain_wait(full(c % STAGES), (c / STAGES) & 1, tmo, a.status);
+            if (g < total) {  // aborted: let the loads in flight land before exiting
+                for (int c = g; c < loaded; ++c)
+                    drain_wait(full(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
         }
     } else if (warp == 1) {
@@ -200,31 +227,38 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
             int issued = 0;
-            for (int j = 0; j < n; ++j) {
-                const int st = j % STAGES;
-                const uint32_t ph = (j / STAGES) & 1;
+            for (int g = 0; g < total; ++g) {
+                const int st = g % kStages;
+                const uint32_t ph = (g / kStages) & 1;
+                const int k = g / d, c = g % d, b = k & 1;
+                if (c == 0 && k >= 2 &&
+                    !mbar_wait(acc_empty(b), ((k >> 1) + 1) & 1, abort_flag, tmo, a.status,
+                               SITE_MMA_ACC))
+                    break;
                 if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_MMA_FULL)) break;
                 if (!mbar_wait(ready(st), ph, abort_flag, tmo, a.status, SITE_MMA_READY)) break;
                 tc_fence_after();
                 const uint32_t sb = base + st * kStageBytes;
+                const uint32_t dcol = tmem_base + b * kAccCols;
 #pragma unroll
                 for (int s = 0; s < 4; ++s) {
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
+                    for (int kk = 0; kk < 2; ++kk) {
                         const uint64_t ad =
-                            smem_desc_sw64(sb + s * kTileT * kRowBytes + k * 32, 8 * kRowBytes);
+                            smem_desc_sw64(sb + s * kTileT * kRowBytes + kk * 32, 8 * kRowBytes);
                         const uint64_t bd = smem_desc_sw64(
-                            sb + kResBytes + kXBytes + s * kWRows * kRowBytes + k * 32,
+                            sb + kResBytes + kXBytes + s * kWRows * kRowBytes + kk * 32,
                             8 * kRowBytes);
-                        tc_mma_bf16(tmem_d, ad, bd, kIdesc, (j | s | k) != 0);
+                        tc_mma_bf16(dcol, ad, bd, kIdesc, (c | s | kk) != 0);
                     }
                 }
                 tc_commit(mma_done(st));
-                issued = j + 1;
+                if (c == d - 1) tc_commit(acc_full(b));
+                issued = g + 1;
             }
-            if (issued > 0 && issued < n) {  // aborted: let the issued MMAs finish
+            if (issued > 0 && issued < total) {  // aborted: let the issued MMAs finish
                 const int c = issued - 1;
-                drain_wait(mma_done(c % STAGES), (c / STAGES) & 1, tmo, a.status);
+                drain_wait(mma_done(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
         }
     } else {
@@ -232,41 +266,118 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
         const int t = q * 32 + lane;
-        const long long gt = t0 + t;
-        const bool valid = gt < a.T;
-        Coefs cf;
-        if (MODE != PRE_ONLY) {
-            float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
-            float4 cv[4] = {pv, pv, pv, pv};
-            if (valid) {
-                pv = __ldg(reinterpret_cast<const float4 *>(a.post) + gt);
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    cv[j] = __ldg(reinterpret_cast<const float4 *>(a.comb) + gt * 4 + j);
-            }
-            const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
-#pragma unroll
-            for (int s = 0; s < 4; ++s) cf.post2[s] = f2_pack(ps[s], ps[s]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float cs[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
-#pragma unroll
-                for (int s = 0; s < 4; ++s) cf.comb2[j][s] = f2_pack(cs[s], cs[s]);
-            }
-        }
-        if (MODE == FUSED_SHIFTED) {
-            float4 lv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (valid) lv = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt);
-            const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) cf.pre2[j] = f2_pack(ls[j], ls[j]);
-        }
-        uint64_t ssq2 = 0, ssql2 = 0;
         const uint32_t swz = (t >> 1) & 3;
-        for (int j = 0; j < n; ++j) {
-            const int st = j % STAGES;
-            const uint32_t ph = (j / STAGES) & 1;
-            if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_WORK_FULL)) break;
+        Coefs cf;
+        bool valid = false;
+        uint64_t ssq2 = 0, ssql2 = 0;
+        float pend_ssq = 0.f, pend_ssql = 0.f;
+        int pend_k = -1;
+        bool aborted = false;
+
+        // epilogue of item kp: 24 partial mixes (hi + lo) and the two partial
+        // sums of squares per token, to the workspace; frees its accumulator.
+        // Half 1 hands its sums to half 0 through shared memory buffer kp & 1,
+        // guarded by mbarriers (bounded waits only, so an abort cannot strand
+        // a warp at a barrier).
+        auto epilogue = [&](int kp) {
+            const int b = kp & 1;
+            float *sx = ssq_x + b * 2 * kTileT;
+            if (half == 1) {
+                const bool free_ok = kp < 2 || mbar_wait(ssq_empty(b), ((kp >> 1) + 1) & 1,
+                                                         abort_flag, tmo, a.status,
+                                                         SITE_EPI_SSQ_FREE);
+                if (free_ok) {
+                    sx[t] = pend_ssq;
+                    sx[kTileT + t] = pend_ssql;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ssq_full(b));
+                return;
+            }
+            const Item it = item_of(kp, n_slices);
+            const long long gt = static_cast<long long>(it.tile) * kTileT + t;
+            const bool got_ssq = mbar_wait(ssq_full(b), (kp >> 1) & 1, abort_flag, tmo, a.status,
+                                           SITE_EPI_SSQ);
+            const float ssq_other = sx[t], ssql_other = sx[kTileT + t];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ssq_empty(b));
+            const bool ok = !aborted && got_ssq &&
+                            mbar_wait(acc_full(b), (kp >> 1) & 1, abort_flag, tmo, a.status,
+                                      SITE_EPI_ACC);
+            tc_fence_after();
+            uint32_t v[48];
+            const uint32_t row = tmem_base + b * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
+            tmem_ld16(row + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+            tmem_ld16(row + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+            tmem_ld16(row + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+            tmem_ld_wait();
+            tc_fence_before();
+            if (gt < a.T && ok) {
+                float out[kPartStride];
+#pragma unroll
+                for (int i = 0; i < 24; ++i)
+                    out[i] = __uint_as_float(v[i]) + __uint_as_float(v[24 + i]);
+                out[24] = pend_ssq + ssq_other;
+                out[25] = pend_ssql + ssql_other;
+                out[26] = 0.f;
+                out[27] = 0.f;
+                float4 *dst = reinterpret_cast<float4 *>(
+                    a.partials + (static_cast<size_t>(it.slice) * a.T + gt) * kPartStride);
+#pragma unroll
+                for (int i = 0; i < kPartStride / 4; ++i)
+                    dst[i] = make_float4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty(b));
+        };
+
+        for (int g = 0; g < total; ++g) {
+            const int st = g % kStages;
+            const uint32_t ph = (g / kStages) & 1;
+            const int k = g / d, c = g % d;
+            if (c == 0) {
+                // new item: park the previous item's sums, load this tile's coefficients
+                if (k > 0) {
+                    pend_ssq = f2_lo(ssq2) + f2_hi(ssq2);
+                    pend_ssql = f2_lo(ssql2) + f2_hi(ssql2);
+                    pend_k = k - 1;
+                }
+                ssq2 = 0;
+                ssql2 = 0;
+                const Item it = item_of(k, n_slices);
+                const long long gt = static_cast<long long>(it.tile) * kTileT + t;
+                valid = gt < a.T;
+                if (MODE != PRE_ONLY) {
+                    float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 cv[4] = {pv, pv, pv, pv};
+                    if (valid) {
+                        pv = __ldg(reinterpret_cast<const float4 *>(a.post) + gt);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            cv[j] = __ldg(reinterpret_cast<const float4 *>(a.comb) + gt * 4 + j);
+                    }
+                    const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) cf.post2[s] = f2_pack(ps[s], ps[s]);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float cs[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) cf.comb2[j][s] = f2_pack(cs[s], cs[s]);
+                    }
+                }
+                if (MODE == FUSED_SHIFTED) {
+                    float4 lv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (valid) lv = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt);
+                    const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cf.pre2[j] = f2_pack(ls[j], ls[j]);
+                }
+            }
+            if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_WORK_FULL)) {
+                aborted = true;
+                break;
+            }
             const uint32_t sb = base + st * kStageBytes;
             if (valid) {
 #pragma unroll
@@ -300,78 +411,49 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(ready(st));
-        }
-        // ---- epilogue: sums of squares (half 0 + half 1), mixes from TMEM
-        const float ssq = f2_lo(ssq2) + f2_hi(ssq2);
-        const float ssql = f2_lo(ssql2) + f2_hi(ssql2);
-        if (half == 1) {
-            ssq_x[t] = ssq;
-            ssql_x[t] = ssql;
-        }
-        named_bar_sync(1, 256);
-        if (half == 0) {
-            const int c = n - 1;
-            const bool ok = mbar_wait(mma_done(c % STAGES), (c / STAGES) & 1, abort_flag, tmo,
-                                      a.status, SITE_EPI_MMA);
-            tc_fence_after();
-            uint32_t v[48];
-            const uint32_t row = tmem_d + (static_cast<uint32_t>(q * 32) << 16);
-            tmem_ld16(row + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-            tmem_ld16(row + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-            tmem_ld16(row + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            if (valid && ok) {
-                float out[kPartStride];
-#pragma unroll
-                for (int i = 0; i < 24; ++i)
-                    out[i] = __uint_as_float(v[i]) + __uint_as_float(v[24 + i]);
-                out[24] = ssq + ssq_x[t];
-                out[25] = ssql + ssql_x[t];
-                out[26] = 0.f;
-                out[27] = 0.f;
-                float4 *dst = reinterpret_cast<float4 *>(
-                    a.partials + (static_cast<size_t>(slice) * a.T + gt) * kPartStride);
-#pragma unroll
-                for (int i = 0; i < kPartStride / 4; ++i)
-                    dst[i] = make_float4(out[4 * i], out[4 * i + 1], out[4 * i + 2],
-                                         out[4 * i + 3]);
+            if (c == 0 && pend_k >= 0) {
+                epilogue(pend_k);
+                pend_k = -1;
             }
         }
+        // the last item's epilogue (after an abort it only frees the warps)
+        pend_ssq = f2_lo(ssq2) + f2_hi(ssq2);
+        pend_ssql = f2_lo(ssql2) + f2_hi(ssql2);
+        if (pend_k >= 0) epilogue(pend_k);   // aborted before the deferred point
+        epilogue(n_local - 1);
     }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem_d, kTmemCols);
+        tmem_dealloc(tmem_base, 2 * kAccCols);
     }
 }
 
-template <int MODE, int STAGES>
+template <int MODE>
 cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtensorMap &rout,
-                     const CUtensorMap &li, const StreamArgs &a, int n_slices, int n_tiles,
-                     cudaStream_t s) {
-    constexpr int smem = kSmemUsed(STAGES) + 1024;
-    auto kern = stream_kernel<MODE, STAGES>;
+                     const CUtensorMap &li, const StreamArgs &a, int n_slices, int n_items,
+                     int grid, cudaStream_t s) {
+    constexpr int smem = kSmemUsed + 1024;
+    auto kern = stream_kernel<MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(n_slices, n_tiles), kStreamThreads, smem, s>>>(res, x, rout, li, a);
+    kern<<<grid, kStreamThreads, smem, s>>>(res, x, rout, li, a, n_slices, n_items);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t stream_smem_bytes(int stages) { return kSmemUsed(stages) + 1024; }
+size_t stream_smem_bytes() { return kSmemUsed + 1024; }
 
-cudaError_t launch_stream(int mode, int stages, const CUtensorMap &res, const CUtensorMap &x,
+cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x,
                           const CUtensorMap &rout, const CUtensorMap &li, const StreamArgs &a,
-                          int n_slices, int n_tiles, cudaStream_t s) {
-    if (stages != 2) return cudaErrorInvalidValue;
+                          int n_slices, int n_items, int grid, cudaStream_t s) {
     switch (mode) {
-        case PRE_ONLY: return launch_t<PRE_ONLY, 2>(res, x, rout, li, a, n_slices, n_tiles, s);
+        case PRE_ONLY: return launch_t<PRE_ONLY>(res, x, rout, li, a, n_slices, n_items, grid, s);
         case FUSED_UNSHIFTED:
-            return launch_t<FUSED_UNSHIFTED, 2>(res, x, rout, li, a, n_slices, n_tiles, s);
+            return launch_t<FUSED_UNSHIFTED>(res, x, rout, li, a, n_slices, n_items, grid, s);
         case FUSED_SHIFTED:
-            return launch_t<FUSED_SHIFTED, 2>(res, x, rout, li, a, n_slices, n_tiles, s);
+            return launch_t<FUSED_SHIFTED>(res, x, rout, li, a, n_slices, n_items, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
