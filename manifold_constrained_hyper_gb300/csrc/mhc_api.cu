@@ -93,16 +93,19 @@ bool aliasing(const Range *outs, int no, const Range *ins, int ni, const void *m
     return false;
 }
 
-// Hidden-slice plan: items of d chunks (slice width 32 * d, d | H/32) spread
-// over kGridCap persistent CTAs; minimise the busiest CTA's work, counting an
-// item's partials (written and read back, ~0.35 of a chunk's bytes) as cost.
-// A pure function of (T, H), so the workspace size is too.
+// Hidden-slice plan: items of d chunks (d | H/32; a slice is d interleaved
+// 32-wide chunks) spread over kGridCap persistent CTAs; minimise the busiest
+// CTA's work, counting an item's partials (written and read back, ~0.35 of
+// a chunk's bytes) as cost. Items of at most 8 chunks keep enough CTAs on
+// one tile for DRAM row locality. A pure function of (T, H), so the
+// workspace size is too.
 void plan(long long T, int H, int *n_slices, int *slice_w) {
     const int chunks = H / kChunk;
     const long long tiles = (T + kTileT - 1) / kTileT;
+    constexpr int kMaxItemChunks = 8;
     double best_cost = -1.0;
-    int best_d = chunks;
-    for (int d = chunks; d >= 1; --d) {
+    int best_d = 1;
+    for (int d = chunks < kMaxItemChunks ? chunks : kMaxItemChunks; d >= 1; --d) {
         if (chunks % d) continue;
         const long long items = tiles * (chunks / d);
         const long long per_cta = (items + kGridCap - 1) / kGridCap;

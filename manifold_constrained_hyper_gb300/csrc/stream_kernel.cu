@@ -102,13 +102,22 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
     mbar_wait(bar, parity, &local, timeout_ns, status, SITE_DRAIN);
 }
 
-// Work item k of this CTA -> (tile, slice).
+// Work item k of this CTA -> (tile, slice). Consecutive CTAs take the
+// slices of one tile, so they stream the same rows at the same time.
 struct Item {
     int tile, slice;
 };
 __device__ __forceinline__ Item item_of(int k, int n_slices) {
     const int i = blockIdx.x + k * gridDim.x;
     return {i / n_slices, i % n_slices};
+}
+
+// First hidden index of chunk c of a slice. Slices interleave chunk by chunk
+// (slice s owns chunks s, s + S, s + 2S, ...), so the CTAs working on one tile
+// read adjacent 64-byte pieces of every row together: DRAM pages are opened
+// once for all of them instead of once per CTA.
+__device__ __forceinline__ int chunk_hidden(int slice, int c, int n_slices) {
+    return (c * n_slices + slice) * kChunk;
 }
 
 template <int MODE>
@@ -178,7 +187,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 const int st = g % kStages;
                 const uint32_t sb = base + st * kStageBytes;
                 const Item it = item_of(g / d, n_slices);
-                const int hc = it.slice * a.slice_w + (g % d) * kChunk;
+                const int hc = chunk_hidden(it.slice, g % d, n_slices);
                 const int t0 = it.tile * kTileT;
                 mbar_arrive_expect_tx(full(st), kLoadBytes);
                 tma_load_3d(sb, &tm_res, hc, t0, 0, full(st), pol_stream);
@@ -197,7 +206,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 if (MODE != PRE_ONLY) {
                     const uint32_t sb = base + st * kStageBytes;
                     const Item it = item_of(g / d, n_slices);
-                    const int hc = it.slice * a.slice_w + (g % d) * kChunk;
+                    const int hc = chunk_hidden(it.slice, g % d, n_slices);
                     const int t0 = it.tile * kTileT;
                     tma_store_3d(&tm_rout, hc, t0, 0, sb, pol_stream);
                     // the collapse is re-read by the finishing kernel: keep it in L2

@@ -47,7 +47,7 @@ def test_sizes_and_plan(lib):
         S, w = ops.plan(T, H)
         assert S * w == H and w % 32 == 0
         assert ops.workspace_bytes(T, H) >= S * T * 28 * 4
-    assert ops.plan(8192, 7168) == (7, 1024)
+    assert ops.plan(8192, 7168) == (28, 256)
 
 
 def test_status_strings(lib):
