@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/mhc.h: argument validation,
 // the hidden-slice plan, TMA tensor-map encoding and kernel dispatch.
 #include <atomic>
+#include <chrono>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -24,7 +25,26 @@ struct DeviceInfo {
     std::once_flag once;
     bool ok = false;
     unsigned int *status = nullptr;
+    int sms = 0;
 };
+
+// Flag value of each shifted call: unique within the process (monotonic),
+// started from a time- and address-derived seed so that stale workspace
+// contents from another process are not mistaken for this call's flags.
+std::atomic<unsigned long long> g_epoch{0};
+std::once_flag g_epoch_once;
+unsigned long long next_epoch() {
+    std::call_once(g_epoch_once, [] {
+        const unsigned long long t = static_cast<unsigned long long>(
+            std::chrono::high_resolution_clock::now().time_since_epoch().count());
+        const unsigned long long a = reinterpret_cast<uintptr_t>(&g_epoch);
+        unsigned long long z = t ^ (a << 17) ^ 0x9E3779B97F4A7C15ull;
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        g_epoch.store((z ^ (z >> 31)) | 1ull);
+    });
+    return g_epoch.fetch_add(1) + 1;
+}
 DeviceInfo g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -41,6 +61,8 @@ mhc_status current_device(DeviceInfo **out) {
         if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
             return;
         if (major != 10 || minor != 3) return;   // the library carries sm_103a code only
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return;
         d.status = device_status_word();
         d.ok = d.status != nullptr;
     });
@@ -119,12 +141,23 @@ void plan(long long T, int H, int *n_slices, int *slice_w) {
     *slice_w = best_d * kChunk;
 }
 
+// Workspace: per-slice partials [S][T][28] fp32, then (each 256-byte
+// aligned) the shifted form's per-slice collapse sums [S][T] fp32 and its
+// publication flags [tiles][S][4] u64.
+size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+size_t partials_bytes(long long T, int S) {
+    return align256(static_cast<size_t>(S) * static_cast<size_t>(T) * kPartStride * sizeof(float));
+}
+size_t ssql_bytes(long long T, int S) {
+    return align256(static_cast<size_t>(S) * static_cast<size_t>(T) * sizeof(float));
+}
+
 size_t workspace_bytes(long long T, int H) {
     if (T <= 0 || !hidden_ok(H)) return 0;
     int S = 0, w = 0;
     plan(T, H, &S, &w);
-    const size_t b = static_cast<size_t>(S) * static_cast<size_t>(T) * kPartStride * sizeof(float);
-    return (b + 255) & ~static_cast<size_t>(255);
+    const size_t tiles = static_cast<size_t>((T + kTileT - 1) / kTileT);
+    return partials_bytes(T, S) + ssql_bytes(T, S) + tiles * S * 4 * sizeof(unsigned long long);
 }
 
 // bf16 [rows.., H] viewed by TMA: dim0 = hidden (box 32, 64-byte swizzle).
@@ -216,13 +249,12 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
 
     int S = 0, w = 0;
     plan(T, H, &S, &w);
-    CUtensorMap m_res, m_x, m_rout, m_li;
+    CUtensorMap m_res, m_x, m_rout;
     if (!encode_res(&m_res, residual, H, T)) return MHC_ERR_CUDA;
-    m_x = m_rout = m_li = m_res;
+    m_x = m_rout = m_res;
     if (fused) {
         if (!encode_2d(&m_x, x, H, T) || !encode_res(&m_rout, residual_out, H, T))
             return MHC_ERR_CUDA;
-        if (mode == FUSED_SHIFTED && !encode_2d(&m_li, layer_input, H, T)) return MHC_ERR_CUDA;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     StreamArgs sa;
@@ -236,11 +268,27 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.H = H;
     sa.slice_w = w;
     sa.timeout_ns = g_timeout_ns.load();
+    sa.ssql = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + partials_bytes(T, S));
+    sa.flags = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) +
+                                                      partials_bytes(T, S) + ssql_bytes(T, S));
+    sa.epoch = mode == FUSED_SHIFTED ? next_epoch() : 0;
+    sa.coef = coef_args(scale, base, params);
+    sa.norm_w = norm_w;
+    sa.nw_bf16 = norm_dtype == MHC_BF16;
+    sa.out32 = (reinterpret_cast<uintptr_t>(layer_input) & 31u) == 0;
+    sa.layer_input = layer_input;
+    sa.pre_out = pre_out;
+    sa.post_out = post_out;
+    sa.comb_out = comb_out;
     const long long tiles = (T + kTileT - 1) / kTileT;
     const long long items = tiles * S;
     if (items > 0x7FFFFFFFLL) return MHC_ERR_UNSUPPORTED;
-    const int grid = static_cast<int>(items < kGridCap ? items : kGridCap);
-    if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, m_li, sa, S,
+    const int cap = dev->sms < kGridCap ? dev->sms : kGridCap;
+    const int grid = static_cast<int>(items < cap ? items : cap);
+    // the shifted form finishes in-kernel: every slice of a tile must be in
+    // flight at once, and an item's collapse must fit its TMEM buffer
+    if (mode == FUSED_SHIFTED && (S > grid || w / kChunk > 8)) return MHC_ERR_UNSUPPORTED;
+    if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, sa, S,
                                                  static_cast<int>(items), grid, st)))
         return s;
     if (t_between_event) {
@@ -262,7 +310,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     fa.comb_out = comb_out;
     fa.T = T;
     fa.H = H;
-    if (mode == FUSED_SHIFTED) return cuda_status(launch_finish_shifted(fa, st));
+    if (mode == FUSED_SHIFTED) return cuda_status(launch_coefficients(fa, st));
     return cuda_status(launch_finish_unshifted(fa, st));
 }
 

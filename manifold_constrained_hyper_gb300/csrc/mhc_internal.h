@@ -22,6 +22,13 @@ constexpr int kPartStride = 28;                     // floats per token per slic
 constexpr int kStreamThreads = 320;                 // TMA warp, MMA warp, 8 workers
 constexpr int kTmemCols = 64;
 
+struct CoefArgs {
+    const float *scale;
+    const float *base;
+    float hc_norm_eps, hc_pre_eps, hc_post_mult, sinkhorn_eps, norm_eps;
+    int sinkhorn_iters;
+};
+
 struct StreamArgs {
     const float *post;       // [T,4]
     const float *comb;       // [T,4,4]
@@ -33,13 +40,16 @@ struct StreamArgs {
     int H;
     int slice_w;             // hidden per slice (multiple of kChunk)
     unsigned long long timeout_ns;
-};
-
-struct CoefArgs {
-    const float *scale;
-    const float *base;
-    float hc_norm_eps, hc_pre_eps, hc_post_mult, sinkhorn_eps, norm_eps;
-    int sinkhorn_iters;
+    // shifted form: the kernel also finishes the boundary
+    float *ssql;                 // [n_slices][T] per-slice sums of the collapse's squares
+    unsigned long long *flags;   // [tiles][n_slices][4] per-call epoch flags
+    unsigned long long epoch;    // this call's flag value
+    CoefArgs coef;
+    const void *norm_w;          // [H] or NULL
+    int nw_bf16;
+    int out32;                   // layer_input 32-byte aligned
+    uint16_t *layer_input;       // [T,H]
+    float *pre_out, *post_out, *comb_out;
 };
 
 struct FinishArgs {
@@ -61,10 +71,10 @@ size_t stream_smem_bytes();
 // Persistent streaming kernel over n_items = tiles x n_slices work items
 // (item i = tile i / n_slices, slice i % n_slices), `grid` CTAs.
 cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x,
-                          const CUtensorMap &rout, const CUtensorMap &li, const StreamArgs &a,
-                          int n_slices, int n_items, int grid, cudaStream_t s);
-cudaError_t launch_finish_shifted(const FinishArgs &a, cudaStream_t s);
+                          const CUtensorMap &rout, const StreamArgs &a, int n_slices, int n_items,
+                          int grid, cudaStream_t s);
 cudaError_t launch_finish_unshifted(const FinishArgs &a, cudaStream_t s);
+cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s);
 cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *post,
                         const float *comb, uint16_t *out, long long T, int H, cudaStream_t s);

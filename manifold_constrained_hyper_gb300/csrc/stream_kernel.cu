@@ -5,39 +5,60 @@
 //      [128][32] (bf16, 64-byte swizzled rows) and bulk-load the chunk's
 //      prepared weight tile [4][48][32] (already in swizzled order);
 //   2. workers update the residual in shared memory (post: the flush-to-zero
-//      FMA chain of the "mhc_boundary" page's residual_update), fold squares
-//      of the updated values into per-token sums, and for the shifted form
-//      write the collapse with the lagged pre (lagged_collapse) over x;
-//   3. TMA-store the updated residual (and the unnormalised collapse);
+//      FMA chain of the "mhc_boundary" page's residual_update) and fold the
+//      squares of the updated values into per-token sums;
+//   3. TMA-store the updated residual;
 //   4. one thread issues 8 tcgen05 MMAs (M=128 tokens, N=48 stacked hi/lo
 //      weight rows, K=16) accumulating the mixer contraction in TMEM.
-// Each item accumulates into one of two TMEM buffers; its epilogue (24
-// partial mixes hi + lo and the partial sums of squares per token, written
-// to the workspace) runs in the workers after they have handled the first
-// chunk of the next item, so neither the MMA nor the stream drains between
-// items. A finishing kernel reduces the slices in a fixed order.
-// Warp roles: warp 0 TMA producer and TMEM owner, warp 1 MMA issuer, warps
-// 2-9 workers (token = 32*(warp%4) + lane: a worker reads the TMEM lanes of
-// its own tokens; warps 2-5 and 6-9 each take two of the four 8-wide units).
+// Slices interleave chunk by chunk and consecutive CTAs take the slices of
+// one tile, so the CTAs of a tile read adjacent pieces of every row together
+// (DRAM row locality). Each item accumulates into one of two TMEM buffers.
+//
+// Finisher warps take every item off the workers' path: they read its
+// accumulator from TMEM and write the 24 partial mixes (hi + lo) and the
+// partial sums of squares of each token to the workspace. In the shifted
+// form ("mhc_boundary" page, lagged_collapse and layer_input_words) the
+// workers also collapse the updated residual with the lagged pre into TMEM;
+// the finishers publish the item with a per-call flag, wait until every
+// slice of the tile has published, and write the layer input
+// bf16((li * rsqrt(sum li^2 / H + eps)) * norm_w) from TMEM. A small kernel
+// forms the coefficients from the partials afterwards.
+//
+// Warps: 0 TMA producer and TMEM owner, 1 MMA issuer, 2-3 idle, 4-11
+// workers (token 32*(warp%4) + lane, so a warp's tokens are its TMEM lane
+// quarter; warps 4-7 take hidden 0-15 of a chunk, 8-11 hidden 16-31), 12-15
+// finishers (token 32*(warp%4) + lane). Registers are redistributed per
+// warpgroup with setmaxnreg: 40 + 184 + 184 + 96 per thread, 64,512 of the
+// 65,536 the CTA is launched with.
+#include "coef.cuh"
 #include "mhc_internal.h"
 #include "ptx.cuh"
 
 namespace mhc {
 namespace {
 
+constexpr int kThreads = 512;
 constexpr int kStages = 4;
 constexpr int kBarOff = kStages * kStageBytes;
-constexpr int kNumBars = 3 * kStages + 8;
-constexpr int kSsqOff = kBarOff + 256;                 // [2 buffers][2 sums][128] fp32
-constexpr int kMiscOff = kSsqOff + 2 * 2 * kTileT * 4;
+constexpr int kAccBufs = 2;                            // accumulator / sums buffers
+constexpr int kLiBufs = 3;                             // shifted: collapse buffers
+constexpr int kNumBars = 3 * kStages + 4 * kAccBufs + 3 + 1;
+constexpr int kSumsOff = kBarOff + 256;                // [buffers][2 halves][2 sums][128] fp32
+constexpr int kMiscOff = kSumsOff + kAccBufs * 2 * 2 * kTileT * 4;
 constexpr int kSmemUsed = kMiscOff + 64;
 constexpr int kAccCols = 64;                           // one accumulator buffer (48 used)
+constexpr int kLiCol = kAccBufs * kAccCols;            // shifted: collapse buffers
+constexpr int kLiCols = 128;                           // 8 chunks x 16 columns
+constexpr int kRegsProducer = 40, kRegsWorker = 184, kRegsFinisher = 96;
 static_assert(kNumBars * 8 <= 256, "barrier area");
+static_assert(128 * (kRegsProducer + kRegsFinisher) + 256 * kRegsWorker <= 65536,
+              "register split exceeds the CTA's allocation");
 
 // Wait-site ids recorded with a timeout.
 enum : int { SITE_PROD_READY = 1, SITE_PROD_MMA = 2, SITE_MMA_FULL = 3, SITE_MMA_READY = 4,
-             SITE_WORK_FULL = 5, SITE_EPI_ACC = 6, SITE_DRAIN = 7, SITE_MMA_ACC = 8,
-             SITE_EPI_SSQ = 9, SITE_EPI_SSQ_FREE = 10 };
+             SITE_WORK_FULL = 5, SITE_FIN_ACC = 6, SITE_DRAIN = 7, SITE_MMA_ACC = 8,
+             SITE_FIN_SUMS = 9, SITE_WORK_SUMS = 10, SITE_TILE_FLAGS = 11, SITE_WORK_LI = 12,
+             SITE_EXIT = 13 };
 
 struct Coefs {
     uint64_t post2[4];       // (post[s], post[s])
@@ -94,6 +115,49 @@ __device__ __forceinline__ uint4 collapse8(const uint4 (&cur)[4], const Coefs &c
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// bf16((li * rstd_li) * w) for 8 values: two separately rounded products.
+__device__ __forceinline__ uint4 rmsnorm8(const uint32_t *li, float rstd_li, const float *w) {
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float lo = __fmul_rn(__fmul_rn(__uint_as_float(li[p] << 16), rstd_li), w[2 * p]);
+        const float hi =
+            __fmul_rn(__fmul_rn(__uint_as_float(li[p] & 0xFFFF0000u), rstd_li), w[2 * p + 1]);
+        o[p] = bf2_pack_rn(f2_pack(lo, hi));
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 8 consecutive norm weights (fp32 or bf16 bits) as fp32.
+__device__ __forceinline__ void norm_w8(const void *nw, int bf16, long long h, float (&w)[8]) {
+    if (bf16) {
+        const uint4 a = ld_global_nc_v4(static_cast<const uint16_t *>(nw) + h);
+        const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[2 * i] = __uint_as_float(ws[i] << 16);
+            w[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+        }
+    } else {
+        const float *p = static_cast<const float *>(nw) + h;
+        const uint4 a = ld_global_nc_v4(p), b = ld_global_nc_v4(p + 4);
+        w[0] = __uint_as_float(a.x); w[1] = __uint_as_float(a.y);
+        w[2] = __uint_as_float(a.z); w[3] = __uint_as_float(a.w);
+        w[4] = __uint_as_float(b.x); w[5] = __uint_as_float(b.y);
+        w[6] = __uint_as_float(b.z); w[7] = __uint_as_float(b.w);
+    }
+}
+
+__device__ __forceinline__ void regs_dec_producer() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
+}
+__device__ __forceinline__ void regs_inc_worker() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsWorker));
+}
+__device__ __forceinline__ void regs_dec_finisher() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsFinisher));
+}
+
 // Bounded wait that ignores the abort flag (drains copies in flight before
 // the CTA exits after an abort).
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
@@ -121,10 +185,10 @@ __device__ __forceinline__ int chunk_hidden(int slice, int c, int n_slices) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kStreamThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_x,
-              const __grid_constant__ CUtensorMap tm_rout, const __grid_constant__ CUtensorMap tm_li,
-              const StreamArgs a, int n_slices, int n_items) {
+              const __grid_constant__ CUtensorMap tm_rout, const StreamArgs a, int n_slices,
+              int n_items) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -134,10 +198,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     auto ready = [&](int st) { return bars + 8u * (kStages + st); };
     auto mma_done = [&](int st) { return bars + 8u * (2 * kStages + st); };
     auto acc_full = [&](int b) { return bars + 8u * (3 * kStages + b); };
-    auto acc_empty = [&](int b) { return bars + 8u * (3 * kStages + 2 + b); };
-    auto ssq_full = [&](int b) { return bars + 8u * (3 * kStages + 4 + b); };
-    auto ssq_empty = [&](int b) { return bars + 8u * (3 * kStages + 6 + b); };
-    float *ssq_x = reinterpret_cast<float *>(gbase + kSsqOff);   // [b][0: ssq, 1: ssql][t]
+    auto acc_empty = [&](int b) { return bars + 8u * (3 * kStages + kAccBufs + b); };
+    auto sums_full = [&](int b) { return bars + 8u * (3 * kStages + 2 * kAccBufs + b); };
+    auto sums_empty = [&](int b) { return bars + 8u * (3 * kStages + 3 * kAccBufs + b); };
+    auto li_empty = [&](int b) { return bars + 8u * (3 * kStages + 4 * kAccBufs + b); };
+    const uint32_t exit_bar = bars + 8u * (3 * kStages + 4 * kAccBufs + kLiBufs);   // every warp is done
+    // per-token sums of squares handed from workers to finishers: [b][half][ssq, ssql][t]
+    float *sums = reinterpret_cast<float *>(gbase + kSumsOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kMiscOff + 16);
 
@@ -153,31 +220,35 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             mbar_init(ready(i), 8);
             mbar_init(mma_done(i), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(acc_full(b), 1);
             mbar_init(acc_empty(b), 4);
-            mbar_init(ssq_full(b), 4);
-            mbar_init(ssq_empty(b), 4);
+            mbar_init(sums_full(b), 8);
+            mbar_init(sums_empty(b), 4);
         }
+        for (int b = 0; b < kLiBufs; ++b) mbar_init(li_empty(b), 4);
+        mbar_init(exit_bar, kThreads / 32);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    constexpr uint32_t kTmemCols = MODE == FUSED_SHIFTED ? 512 : kAccBufs * kAccCols;
+    static_assert(kAccBufs * kAccCols + kLiBufs * kLiCols <= 512, "TMEM columns");
     if (warp == 0) {
-        tmem_alloc(smem_addr(tmem_slot), 2 * kAccCols);
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     if (tid == 32) {
         tma_prefetch_desc(&tm_res);
         if (MODE != PRE_ONLY) { tma_prefetch_desc(&tm_x); tma_prefetch_desc(&tm_rout); }
-        if (MODE == FUSED_SHIFTED) tma_prefetch_desc(&tm_li);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
-        if (lane == 0) {
+    if (warp < 4) {
+        regs_dec_producer();
+        if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer
             const uint64_t pol_stream = policy_evict_first();
             const uint64_t pol_keep = policy_evict_last();
@@ -207,13 +278,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     const uint32_t sb = base + st * kStageBytes;
                     const Item it = item_of(g / d, n_slices);
                     const int hc = chunk_hidden(it.slice, g % d, n_slices);
-                    const int t0 = it.tile * kTileT;
-                    tma_store_3d(&tm_rout, hc, t0, 0, sb, pol_stream);
-                    // the collapse is re-read by the finishing kernel: keep it in L2
-                    if (MODE == FUSED_SHIFTED) tma_store_2d(&tm_li, hc, t0, sb + kResBytes, pol_keep);
+                    tma_store_3d(&tm_rout, hc, it.tile * kTileT, 0, sb, pol_stream);
                     bulk_commit();
                 }
-                // refill the stage of the previous chunk: its stores have had a
+                // refill the stage of the previous chunk: its store has had a
                 // whole chunk to read shared memory
                 if (g >= 1 && loaded < total) {
                     const int gp = g - 1;
@@ -230,18 +298,16 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 for (int c = g; c < loaded; ++c)
                     drain_wait(full(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
             int issued = 0;
             for (int g = 0; g < total; ++g) {
                 const int st = g % kStages;
                 const uint32_t ph = (g / kStages) & 1;
-                const int k = g / d, c = g % d, b = k & 1;
-                if (c == 0 && k >= 2 &&
-                    !mbar_wait(acc_empty(b), ((k >> 1) + 1) & 1, abort_flag, tmo, a.status,
+                const int k = g / d, c = g % d, b = k % kAccBufs;
+                if (c == 0 && k >= kAccBufs &&
+                    !mbar_wait(acc_empty(b), ((k / kAccBufs) + 1) & 1, abort_flag, tmo, a.status,
                                SITE_MMA_ACC))
                     break;
                 if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_MMA_FULL)) break;
@@ -270,87 +336,51 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 drain_wait(mma_done(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
         }
-    } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(exit_bar);
+        if (warp == 0) {
+            // no warp touches TMEM any more: release it
+            drain_wait(exit_bar, 0, tmo, a.status);
+            tc_fence_after();
+            tmem_dealloc(tmem_base, kTmemCols);
+        }
+    } else if (warp < 12) {
         // ---------------------------------------------------- elementwise workers
+        regs_inc_worker();
         const int q = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int half = (warp - 4) >> 2;
         const int t = q * 32 + lane;
         const uint32_t swz = (t >> 1) & 3;
+        const uint32_t li_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + kLiCol + half * 8;
         Coefs cf;
         bool valid = false;
         uint64_t ssq2 = 0, ssql2 = 0;
-        float pend_ssq = 0.f, pend_ssql = 0.f;
-        int pend_k = -1;
-        bool aborted = false;
 
-        // epilogue of item kp: 24 partial mixes (hi + lo) and the two partial
-        // sums of squares per token, to the workspace; frees its accumulator.
-        // Half 1 hands its sums to half 0 through shared memory buffer kp & 1,
-        // guarded by mbarriers (bounded waits only, so an abort cannot strand
-        // a warp at a barrier).
-        auto epilogue = [&](int kp) {
-            const int b = kp & 1;
-            float *sx = ssq_x + b * 2 * kTileT;
-            if (half == 1) {
-                const bool free_ok = kp < 2 || mbar_wait(ssq_empty(b), ((kp >> 1) + 1) & 1,
-                                                         abort_flag, tmo, a.status,
-                                                         SITE_EPI_SSQ_FREE);
-                if (free_ok) {
-                    sx[t] = pend_ssq;
-                    sx[kTileT + t] = pend_ssql;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ssq_full(b));
-                return;
-            }
-            const Item it = item_of(kp, n_slices);
-            const long long gt = static_cast<long long>(it.tile) * kTileT + t;
-            const bool got_ssq = mbar_wait(ssq_full(b), (kp >> 1) & 1, abort_flag, tmo, a.status,
-                                           SITE_EPI_SSQ);
-            const float ssq_other = sx[t], ssql_other = sx[kTileT + t];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ssq_empty(b));
-            const bool ok = !aborted && got_ssq &&
-                            mbar_wait(acc_full(b), (kp >> 1) & 1, abort_flag, tmo, a.status,
-                                      SITE_EPI_ACC);
-            tc_fence_after();
-            uint32_t v[48];
-            const uint32_t row = tmem_base + b * kAccCols + (static_cast<uint32_t>(q * 32) << 16);
-            tmem_ld16(row + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-            tmem_ld16(row + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-            tmem_ld16(row + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            if (gt < a.T && ok) {
-                float out[kPartStride];
-#pragma unroll
-                for (int i = 0; i < 24; ++i)
-                    out[i] = __uint_as_float(v[i]) + __uint_as_float(v[24 + i]);
-                out[24] = pend_ssq + ssq_other;
-                out[25] = pend_ssql + ssql_other;
-                out[26] = 0.f;
-                out[27] = 0.f;
-                float4 *dst = reinterpret_cast<float4 *>(
-                    a.partials + (static_cast<size_t>(it.slice) * a.T + gt) * kPartStride);
-#pragma unroll
-                for (int i = 0; i < kPartStride / 4; ++i)
-                    dst[i] = make_float4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+        // hand item kp's per-token sums to the finishers (buffer kp % kAccBufs)
+        auto hand_over = [&](int kp) {
+            const int b = kp % kAccBufs;
+            if (kp >= kAccBufs)
+                mbar_wait(sums_empty(b), ((kp / kAccBufs) + 1) & 1, abort_flag, tmo, a.status,
+                          SITE_WORK_SUMS);
+            float *sx = sums + (b * 2 + half) * 2 * kTileT;
+            sx[t] = f2_lo(ssq2) + f2_hi(ssq2);
+            sx[kTileT + t] = f2_lo(ssql2) + f2_hi(ssql2);
+            if (MODE == FUSED_SHIFTED) {
+                tmem_st_wait();      // the item's collapse is in TMEM
+                tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty(b));
+            if (lane == 0) mbar_arrive(sums_full(b));
         };
 
-        for (int g = 0; g < total; ++g) {
+        int g = 0;
+        for (; g < total; ++g) {
             const int st = g % kStages;
             const uint32_t ph = (g / kStages) & 1;
             const int k = g / d, c = g % d;
             if (c == 0) {
-                // new item: park the previous item's sums, load this tile's coefficients
-                if (k > 0) {
-                    pend_ssq = f2_lo(ssq2) + f2_hi(ssq2);
-                    pend_ssql = f2_lo(ssql2) + f2_hi(ssql2);
-                    pend_k = k - 1;
-                }
+                // new item: hand over the previous item's sums, load this tile's coefficients
+                if (k > 0) hand_over(k - 1);
                 ssq2 = 0;
                 ssql2 = 0;
                 const Item it = item_of(k, n_slices);
@@ -381,18 +411,23 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) cf.pre2[j] = f2_pack(ls[j], ls[j]);
+                    // the finishers are done with the collapse buffer this item reuses
+                    if (k >= kLiBufs) {
+                        mbar_wait(li_empty(k % kLiBufs), ((k / kLiBufs) + 1) & 1, abort_flag, tmo,
+                                  a.status, SITE_WORK_LI);
+                        tc_fence_after();
+                    }
                 }
             }
-            if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_WORK_FULL)) {
-                aborted = true;
-                break;
-            }
+            if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_WORK_FULL)) break;
             const uint32_t sb = base + st * kStageBytes;
-            if (valid) {
+            const uint32_t li_chunk = li_lane + (k % kLiBufs) * kLiCols + c * 16;
 #pragma unroll
-                for (int uu = 0; uu < 2; ++uu) {
-                    const int u = 2 * half + uu;
-                    const uint32_t off = t * kRowBytes + 16u * (u ^ swz);
+            for (int uu = 0; uu < 2; ++uu) {
+                const int u = 2 * half + uu;
+                const uint32_t off = t * kRowBytes + 16u * (u ^ swz);
+                uint4 li = make_uint4(0u, 0u, 0u, 0u);
+                if (valid) {
                     uint4 r[4];
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
@@ -410,44 +445,216 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             sq_accum(cur[s], ssq2);
                         }
                         if (MODE == FUSED_SHIFTED) {
-                            const uint4 li = collapse8(cur, cf);
-                            st_shared_v4(sb + kResBytes + off, li);
+                            li = collapse8(cur, cf);
                             sq_accum(li, ssql2);
                         }
                     }
                 }
+                // this thread's 8 collapse values of the unit, kept in TMEM
+                if (MODE == FUSED_SHIFTED) tmem_st4(li_chunk + 4 * uu, li);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(ready(st));
-            if (c == 0 && pend_k >= 0) {
-                epilogue(pend_k);
-                pend_k = -1;
-            }
         }
-        // the last item's epilogue (after an abort it only frees the warps)
-        pend_ssq = f2_lo(ssq2) + f2_hi(ssq2);
-        pend_ssql = f2_lo(ssql2) + f2_hi(ssql2);
-        if (pend_k >= 0) epilogue(pend_k);   // aborted before the deferred point
-        epilogue(n_local - 1);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * kAccCols);
+        // the last item (after an abort the finishers only get their barriers)
+        if (total > 0) hand_over(g < total ? g / d : n_local - 1);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(exit_bar);
+    } else {
+        // ---------------------------------------------------- finishers
+        regs_dec_finisher();
+        const int q = warp & 3;
+        const int t = q * 32 + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint64_t pol_out = policy_evict_first();
+        // Item k is published as soon as its accumulator is ready; its layer
+        // input is written one item later, once the tile's other slices have
+        // published too (by then they almost always have).
+        for (int k = 0; k <= n_local; ++k) {
+            if (k < n_local) {
+                const int b = k % kAccBufs;
+                const uint32_t ph = (k / kAccBufs) & 1;
+                const Item it = item_of(k, n_slices);
+                const long long gt = static_cast<long long>(it.tile) * kTileT + t;
+                // partial mixes and sums of squares of the item
+                bool ok = mbar_wait(sums_full(b), ph, abort_flag, tmo, a.status, SITE_FIN_SUMS);
+                ok = mbar_wait(acc_full(b), ph, abort_flag, tmo, a.status, SITE_FIN_ACC) && ok;
+                tc_fence_after();
+                const float *s0 = sums + (b * 2 + 0) * 2 * kTileT;
+                const float *s1 = sums + (b * 2 + 1) * 2 * kTileT;
+                const float ssq = s0[t] + s1[t];
+                const float ssql = s0[kTileT + t] + s1[kTileT + t];
+                uint32_t v[48];
+                const uint32_t acc = tmem_base + b * kAccCols + lane_off;
+                tmem_ld16(acc + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                tmem_ld16(acc + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                tmem_ld16(acc + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(sums_empty(b));
+                    mbar_arrive(acc_empty(b));
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok && gt < a.T) {
+                    float out[kPartStride];
+#pragma unroll
+                    for (int i = 0; i < 24; ++i)
+                        out[i] = __uint_as_float(v[i]) + __uint_as_float(v[24 + i]);
+                    out[24] = ssq;
+                    out[25] = ssql;
+                    out[26] = 0.f;
+                    out[27] = 0.f;
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        a.partials + (static_cast<size_t>(it.slice) * a.T + gt) * kPartStride);
+#pragma unroll
+                    for (int i = 0; i < kPartStride / 4; ++i)
+                        dst[i] = make_float4(out[4 * i], out[4 * i + 1], out[4 * i + 2],
+                                             out[4 * i + 3]);
+                    if (MODE == FUSED_SHIFTED)
+                        a.ssql[static_cast<size_t>(it.slice) * a.T + gt] = ssql;
+                }
+                // publish this quarter of the item to the tile's other slices
+                if (MODE == FUSED_SHIFTED) {
+                    __syncwarp();
+                    if (lane == 0)
+                        flag_release(a.flags +
+                                         (static_cast<long long>(it.tile) * n_slices + it.slice) * 4 + q,
+                                     a.epoch);
+                }
+            }
+            if (MODE != FUSED_SHIFTED || k == 0) continue;
+
+            // ---- layer input of item kn = k - 1
+            const int kn = k - 1, lb = kn % kLiBufs;
+            const Item it = item_of(kn, n_slices);
+            const long long gt = static_cast<long long>(it.tile) * kTileT + t;
+            bool ok = !*abort_flag;
+            // every slice of the tile published: rstd of each token's collapse
+            if (ok && a.norm_w != nullptr) {
+                const unsigned long long *fl = a.flags + static_cast<long long>(it.tile) * n_slices * 4;
+                uint64_t t_start = 0;
+                for (int f = lane; f < n_slices * 4 && ok; f += 32) {
+                    while (flag_acquire(fl + f) != a.epoch) {
+                        if (*abort_flag) { ok = false; break; }
+                        const uint64_t now = globaltimer_ns();
+                        if (t_start == 0) {
+                            t_start = now;
+                        } else if (now - t_start > tmo) {
+                            record_failure(a.status, 7, SITE_TILE_FLAGS);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        nanosleep_ns(256);
+                    }
+                }
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            float rstd_li = 0.f;
+            if (ok && gt < a.T && a.norm_w != nullptr) {
+                // independent loads, added in slice order
+                const float *pp = a.ssql + gt;
+                const size_t step = static_cast<size_t>(a.T);
+                float sl = 0.f;
+                for (int s2 = 0; s2 < n_slices; s2 += 16) {
+                    float vv[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) vv[i] = s2 + i < n_slices ? pp[(s2 + i) * step] : 0.f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (s2 + i < n_slices) sl += vv[i];
+                }
+                rstd_li = rsqrtf(__fdiv_rn(sl, static_cast<float>(a.H)) + a.coef.norm_eps);
+            }
+            // 32 hidden per chunk; lane l fetches norm weight l of the chunk
+            // (one coalesced load per warp) and the values go round by shuffle
+            auto nw_lane = [&](int c) -> float {
+                if (a.norm_w == nullptr) return 0.f;
+                const long long h = chunk_hidden(it.slice, c, n_slices) + lane;
+                if (a.nw_bf16)
+                    return __uint_as_float(static_cast<uint32_t>(
+                                               __ldg(static_cast<const uint16_t *>(a.norm_w) + h))
+                                           << 16);
+                return __ldg(static_cast<const float *>(a.norm_w) + h);
+            };
+            const uint32_t li = tmem_base + lane_off + kLiCol + lb * kLiCols;
+            float w_next = nw_lane(0);
+            for (int c = 0; c < d; ++c) {
+                const float w_cur = w_next;
+                if (c + 1 < d) w_next = nw_lane(c + 1);
+                uint32_t w16[16];
+                tmem_ld16(li + c * 16, w16);
+                tmem_ld_wait();
+                const long long h0 = chunk_hidden(it.slice, c, n_slices);
+                uint16_t *dst = a.layer_input + gt * a.H + h0;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {            // the two 16-wide halves
+                    uint32_t o[8];
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) {
+                        const uint32_t wd = w16[8 * hh + p];
+                        const int e = 16 * hh + 2 * p;
+                        // every lane takes part in the shuffles
+                        const float w_lo = __shfl_sync(0xffffffffu, w_cur, e);
+                        const float w_hi = __shfl_sync(0xffffffffu, w_cur, e + 1);
+                        if (a.norm_w != nullptr) {
+                            const float lo = __fmul_rn(__fmul_rn(__uint_as_float(wd << 16), rstd_li), w_lo);
+                            const float hi =
+                                __fmul_rn(__fmul_rn(__uint_as_float(wd & 0xFFFF0000u), rstd_li), w_hi);
+                            o[p] = bf2_pack_rn(f2_pack(lo, hi));
+                        } else {
+                            o[p] = wd;
+                        }
+                    }
+                    if (ok && gt < a.T) {
+                        const uint4 o0 = make_uint4(o[0], o[1], o[2], o[3]);
+                        const uint4 o1 = make_uint4(o[4], o[5], o[6], o[7]);
+                        if (a.out32) {
+                            st_global_v8(dst + 16 * hh, o0, o1, pol_out);
+                        } else {
+                            st_global_v4(dst + 16 * hh, o0, pol_out);
+                            st_global_v4(dst + 16 * hh + 8, o1, pol_out);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(li_empty(lb));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(exit_bar);
     }
 }
 
 template <int MODE>
 cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtensorMap &rout,
-                     const CUtensorMap &li, const StreamArgs &a, int n_slices, int n_items,
-                     int grid, cudaStream_t s) {
+                     const StreamArgs &a, int n_slices, int n_items, int grid, cudaStream_t s) {
     constexpr int smem = kSmemUsed + 1024;
     auto kern = stream_kernel<MODE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kStreamThreads, smem, s>>>(res, x, rout, li, a, n_slices, n_items);
-    return cudaGetLastError();
+    if (MODE != FUSED_SHIFTED) {
+        kern<<<grid, kThreads, smem, s>>>(res, x, rout, a, n_slices, n_items);
+        return cudaGetLastError();
+    }
+    // the shifted form's CTAs wait on one another: launch them co-resident
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, res, x, rout, a, n_slices, n_items);
 }
 
 }  // namespace
@@ -455,14 +662,14 @@ cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtenso
 size_t stream_smem_bytes() { return kSmemUsed + 1024; }
 
 cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x,
-                          const CUtensorMap &rout, const CUtensorMap &li, const StreamArgs &a,
-                          int n_slices, int n_items, int grid, cudaStream_t s) {
+                          const CUtensorMap &rout, const StreamArgs &a, int n_slices, int n_items,
+                          int grid, cudaStream_t s) {
     switch (mode) {
-        case PRE_ONLY: return launch_t<PRE_ONLY>(res, x, rout, li, a, n_slices, n_items, grid, s);
+        case PRE_ONLY: return launch_t<PRE_ONLY>(res, x, rout, a, n_slices, n_items, grid, s);
         case FUSED_UNSHIFTED:
-            return launch_t<FUSED_UNSHIFTED>(res, x, rout, li, a, n_slices, n_items, grid, s);
+            return launch_t<FUSED_UNSHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
         case FUSED_SHIFTED:
-            return launch_t<FUSED_SHIFTED>(res, x, rout, li, a, n_slices, n_items, grid, s);
+            return launch_t<FUSED_SHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
