@@ -234,6 +234,17 @@ mhc_status mhc_debug_unarmed_wait(void *stream);
  * NULL clears a pending event. */
 void mhc_debug_record_between(void *event);
 
+/* Test hook for the coefficients' reciprocal (the "mhc_boundary" page's rcp:
+ * hardware approximation plus one Newton-Raphson step): compares it with the
+ * correctly rounded fp32 reciprocal for the bit patterns first_bits ..
+ * first_bits + count - 1 (no wrap past 0xFFFFFFFF, else MHC_ERR_SHAPE).
+ * result: device pointer to two u64, 8-byte aligned, set by the caller to
+ * {0, ~0} beforehand; result[0] += the number of differing patterns,
+ * result[1] = min(its value, the smallest differing pattern). Enqueued on
+ * `stream`. The pages have no counterpart. */
+mhc_status mhc_debug_rcp_check(uint32_t first_bits, uint64_t count, unsigned long long *result,
+                               void *stream);
+
 /* Slice plan chosen for (T, H): writes the number of hidden slices and the
  * slice width. For tests and the benchmark's byte accounting. */
 mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width);

@@ -1,6 +1,6 @@
 // Weight preparation, the standalone residual update, the finishing kernels
-// of the boundary (slice reduction, coefficients with a warp-shuffle
-// Sinkhorn, layer RMSNorm of the collapse), the device status word and the
+// of the boundary (slice reduction and coefficients; for the unshifted form
+// the collapse and its RMSNorm after them), the device status word and the
 // wait-timeout probe.
 #include <cuda_bf16.h>
 
@@ -100,43 +100,62 @@ __global__ void post_kernel(const uint16_t *__restrict__ x, const uint16_t *__re
     }
 }
 
-// ------------------------------------------------------------ coefficients (shifted)
-// One warp per token: slice reduction of the partial mixes and sum of
-// squares, then pre / post / comb. The shifted boundary's streaming kernel
-// has already written the layer input.
-__global__ void __launch_bounds__(256) coefficients_kernel(const FinishArgs a) {
-    const int lane = threadIdx.x & 31;
-    const long long t = blockIdx.x * 8LL + (threadIdx.x >> 5);
-    if (t >= a.T) return;
-    const float v = reduce_slices(a.partials, a.n_slices, a.T, t, lane_slot(lane));
-    coefficients_warp(v, lane, a.coef, a.H, t, a.pre_out, a.post_out, a.comb_out);
-}
+// ------------------------------------------------------------ coefficients
+// 32 tokens (a quarter of a tile) per block. Warp m (m < 25) sums value m of
+// the block's tokens over the hidden slices, lane = token, in slice order with
+// every load in flight at once (each load a 128-byte row of the item's
+// value-major partials); then warp 0 forms the 32 tokens' pre / post / comb,
+// one thread per token. Launched as a programmatic dependent of the streaming
+// kernel: blocks may start early and wait here for its completion.
+constexpr int kCoefTokens = 32;
+constexpr int kCoefThreads = kPartVals * 32;
 
-// ------------------------------------------------------------ finish (unshifted)
-// One 128-thread block per token: warp 0 reduces the slices and forms the
-// coefficients; then all threads collapse the token's 4 streams with this
-// boundary's pre into shared memory, reduce the collapse's sum of squares
-// in a fixed order, and write the normalised layer input.
-constexpr int kFinThreads = 128;
-
-__global__ void __launch_bounds__(kFinThreads) finish_unshifted_kernel(const FinishArgs a) {
-    extern __shared__ uint4 li_s[];            // [H/8]
-    __shared__ float pre_s[4];
-    __shared__ float red_s[kFinThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long t = blockIdx.x;
-    if (warp == 0) {
-        const float v = reduce_slices(a.partials, a.n_slices, a.T, t, lane_slot(lane));
-        const float pre = coefficients_warp(v, lane, a.coef, a.H, t, a.pre_out, a.post_out,
-                                            a.comb_out);
-        if (lane < 4) pre_s[lane] = pre;
+__global__ void __launch_bounds__(kCoefThreads, 2) coefficients_kernel(const FinishArgs a) {
+    __shared__ float red[kPartVals][kCoefTokens];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long t0 = static_cast<long long>(blockIdx.x) * kCoefTokens;
+    const long long t = t0 + lane;
+    const long long tile = t0 / kTileT;
+    const int tin = static_cast<int>(t0 % kTileT) + lane;
+    griddep_wait();
+    if (t < a.T) {
+        const float *p = a.partials + (tile * a.n_slices * kPartVals + warp) * kTileT + tin;
+        const long long step = static_cast<long long>(kPartVals) * kTileT;
+        float v = 0.f;
+        for (int s = 0; s < a.n_slices; s += 32) {
+            float w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w[i] = s + i < a.n_slices ? __ldg(p + (s + i) * step) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (s + i < a.n_slices) v += w[i];
+        }
+        red[warp][lane] = v;
     }
     __syncthreads();
-    const uint64_t p2[4] = {f2_pack(pre_s[0], pre_s[0]), f2_pack(pre_s[1], pre_s[1]),
-                            f2_pack(pre_s[2], pre_s[2]), f2_pack(pre_s[3], pre_s[3])};
+    if (warp == 0 && t < a.T)
+        coefficients_thread(&red[0][lane], kCoefTokens, a.coef, a.H, t, a.pre_out, a.post_out,
+                            a.comb_out);
+}
+
+// ------------------------------------------------------------ collapse (unshifted)
+// One 128-thread block per token, after the coefficients: collapse the
+// token's 4 updated streams with this boundary's pre into shared memory,
+// reduce the collapse's sum of squares in a fixed order, and write the
+// normalised layer input.
+constexpr int kColThreads = 128;
+
+__global__ void __launch_bounds__(kColThreads) collapse_unshifted_kernel(const FinishArgs a) {
+    extern __shared__ uint4 li_s[];            // [H/8]
+    __shared__ float red_s[kColThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long t = blockIdx.x;
+    const float4 pv = reinterpret_cast<const float4 *>(a.pre_out)[t];
+    const uint64_t p2[4] = {f2_pack(pv.x, pv.x), f2_pack(pv.y, pv.y), f2_pack(pv.z, pv.z),
+                            f2_pack(pv.w, pv.w)};
     const int units = a.H / 8;
     uint64_t sq2 = 0;
-    for (int u = tid; u < units; u += kFinThreads) {
+    for (int u = tid; u < units; u += kColThreads) {
         uint32_t cs[4][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -157,7 +176,7 @@ __global__ void __launch_bounds__(kFinThreads) finish_unshifted_kernel(const Fin
     }
     uint16_t *row = a.layer_input + t * a.H;
     if (a.norm_w == nullptr) {
-        for (int u = tid; u < units; u += kFinThreads)
+        for (int u = tid; u < units; u += kColThreads)
             *reinterpret_cast<uint4 *>(row + 8LL * u) = li_s[u];
         return;
     }
@@ -168,11 +187,39 @@ __global__ void __launch_bounds__(kFinThreads) finish_unshifted_kernel(const Fin
     __syncthreads();
     float tot = 0.f;
 #pragma unroll
-    for (int w = 0; w < kFinThreads / 32; ++w) tot += red_s[w];
+    for (int w = 0; w < kColThreads / 32; ++w) tot += red_s[w];
     const float rstd_li = rsqrtf(__fdiv_rn(tot, static_cast<float>(a.H)) + a.coef.norm_eps);
-    for (int u = tid; u < units; u += kFinThreads)
+    for (int u = tid; u < units; u += kColThreads)
         *reinterpret_cast<uint4 *>(row + 8LL * u) =
             norm8(li_s[u], rstd_li, a.norm_w, a.nw_bf16, 8LL * u);
+}
+
+// ------------------------------------------------------------ reciprocal check
+// Counts the bit patterns in [first, first + count) whose rcp_nr differs from
+// the correctly rounded reciprocal; out[0] += count, out[1] = min(pattern).
+__global__ void rcp_check_kernel(uint32_t first, unsigned long long count,
+                                 unsigned long long *out) {
+    unsigned long long bad = 0, first_bad = ~0ull;
+    const unsigned long long stride = static_cast<unsigned long long>(gridDim.x) * blockDim.x;
+    for (unsigned long long i = blockIdx.x * static_cast<unsigned long long>(blockDim.x) + threadIdx.x;
+         i < count; i += stride) {
+        const uint32_t b = first + static_cast<uint32_t>(i);
+        const float x = __uint_as_float(b);
+        if (__float_as_uint(rcp_nr(x)) != __float_as_uint(__frcp_rn(x))) {
+            ++bad;
+            if (b < first_bad) first_bad = b;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        bad += __shfl_xor_sync(0xffffffffu, bad, o);
+        const unsigned long long f = __shfl_xor_sync(0xffffffffu, first_bad, o);
+        first_bad = f < first_bad ? f : first_bad;
+    }
+    if ((threadIdx.x & 31) == 0 && bad) {
+        atomicAdd(out, bad);
+        atomicMin(out + 1, first_bad);
+    }
 }
 
 // ------------------------------------------------------------ timeout probe
@@ -216,20 +263,33 @@ cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *pos
 }
 
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s) {
-    const long long blocks = (a.T + 7) / 8;
-    coefficients_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((a.T + kCoefTokens - 1) / kCoefTokens));
+    cfg.blockDim = dim3(kCoefThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, coefficients_kernel, a);
 }
 
-cudaError_t launch_finish_unshifted(const FinishArgs &a, cudaStream_t s) {
+cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(a.H) * 2;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(finish_unshifted_kernel,
+        cudaError_t e = cudaFuncSetAttribute(collapse_unshifted_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    finish_unshifted_kernel<<<static_cast<unsigned>(a.T), kFinThreads, smem, s>>>(a);
+    collapse_unshifted_kernel<<<static_cast<unsigned>(a.T), kColThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rcp_check(uint32_t first, unsigned long long count, unsigned long long *out,
+                             cudaStream_t s) {
+    rcp_check_kernel<<<152 * 8, 256, 0, s>>>(first, count, out);
     return cudaGetLastError();
 }
 

@@ -7,88 +7,83 @@
 namespace mhc {
 
 // ------------------------------------------------------------ coefficients
+// Reciprocal of a positive normal x whose reciprocal is also normal, as the
+// "mhc_boundary" page's rcp: the hardware approximation y0 refined by one
+// Newton-Raphson step in fused multiply-add form, y0 + y0 * (1 - x * y0)
+// (Markstein); 1 - x * y0 is exact. The library checks on the GPU that this
+// equals the correctly rounded reciprocal for every such x.
+static __device__ __forceinline__ float rcp_nr(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return fmaf(y, fmaf(-x, y, 1.0f), y);
+}
+
 static __device__ __forceinline__ float sigmoid_clamped(float v) {
     // 1 / min(1 + exp(-v), 2^126) ("mhc_boundary" page, sigmoid)
-    return __frcp_rn(fminf(1.0f + expf(-v), 0x1p126f));
+    return rcp_nr(fminf(1.0f + expf(-v), 0x1p126f));
 }
 
-// Lane map of one token's warp: lanes 0-3 pre (mix 0-3), 4-7 post (mix 4-7),
-// lane 8 the 4H sum of squares, lane 9 the collapse's sum of squares, lanes
-// 16-31 comb (mix 8-23, lane 16 + 4i + k = row i, column k).
-static __device__ __forceinline__ int lane_slot(int lane) {
-    if (lane < 8) return lane;
-    if (lane == 8) return 24;
-    if (lane == 9) return 25;
-    if (lane >= 16) return lane - 8;
-    return -1;
-}
-
-// Sum of one token's slice partials in slice order (fixed, deterministic).
-static __device__ __forceinline__ float reduce_slices(const float *__restrict__ partials, int n_slices,
-                                               long long T, long long t, int slot) {
-    float v = 0.f;
-    if (slot >= 0) {
-        // independent loads, added in slice order
-        const float *p = partials + t * kPartStride + slot;
-        const long long step = T * kPartStride;
-        int s = 0;
-        for (; s + 8 <= n_slices; s += 8) {
-            float w[8];
+// Coefficients of token t formed by one thread from the token's reduced
+// values v[i * stride]: i = 0..23 the mixes, 24 the 4H sum of squares; writes
+// pre / post / comb. Order of operations as in the "mhc_boundary" page
+// (coefficients, sinkhorn, col_normalize): pre = sigmoid(m0 * s0 + b) + eps,
+// post = sigmoid(m1 * s1 + b) * post_mult, comb = row softmax (multiplied by
+// the reciprocal of the row sum, plus eps), one column normalisation, then
+// iters - 1 times a row and a column normalisation; column sums pair rows
+// (0, 1) and (2, 3).
+static __device__ __forceinline__ void coefficients_thread(const float *v, int stride,
+                                                           const CoefArgs &c, int H, long long t,
+                                                           float *pre_out, float *post_out,
+                                                           float *comb_out) {
+    const float rstd =
+        rsqrtf(__fdiv_rn(v[24 * stride], static_cast<float>(4 * H)) + c.hc_norm_eps);
+    const float s0 = __ldg(c.scale + 0), s1 = __ldg(c.scale + 1), s2 = __ldg(c.scale + 2);
+    float pp[4], po[4];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = __ldg(p + (s + i) * step);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v += w[i];
-        }
-        for (; s < n_slices; ++s) v += __ldg(p + s * step);
+    for (int i = 0; i < 4; ++i) {
+        pp[i] = sigmoid_clamped(fmaf(v[i * stride] * rstd, s0, __ldg(c.base + i))) + c.hc_pre_eps;
+        po[i] = sigmoid_clamped(fmaf(v[(4 + i) * stride] * rstd, s1, __ldg(c.base + 4 + i))) *
+                c.hc_post_mult;
     }
-    return v;
-}
-
-// Coefficients of token t from its reduced value v (lane map above); writes
-// pre / post / comb. Returns pre[lane & 3] in lanes 0-3 (undefined elsewhere).
-// Order of operations as in the "mhc_boundary" page (coefficients, sinkhorn,
-// col_normalize); the Sinkhorn runs on 16 lanes with shuffles.
-static __device__ __forceinline__ float coefficients_warp(float v, int lane, const CoefArgs &c, int H, long long t,
-                                   float *pre_out, float *post_out, float *comb_out) {
-    const unsigned full = 0xffffffffu;
-    const float ssq = __shfl_sync(full, v, 8);
-    const float rstd = rsqrtf(__fdiv_rn(ssq, static_cast<float>(4 * H)) + c.hc_norm_eps);
-    const int slot = lane_slot(lane);
-    const float m = v * rstd;
-    float pre = 0.f;
-    if (lane < 4) {
-        pre = sigmoid_clamped(fmaf(m, __ldg(c.scale + 0), __ldg(c.base + slot))) + c.hc_pre_eps;
-        pre_out[t * 4 + lane] = pre;
-    } else if (lane < 8) {
-        const float p = sigmoid_clamped(fmaf(m, __ldg(c.scale + 1), __ldg(c.base + slot)));
-        post_out[t * 4 + lane - 4] = p * c.hc_post_mult;
-    }
-    // comb lanes 16..31; the other lanes follow the shuffles on dummy values
-    const bool comb_lane = lane >= 16;
-    const float l = comb_lane ? fmaf(m, __ldg(c.scale + 2), __ldg(c.base + slot)) : 0.f;
-    const int rb = lane & ~3;   // first lane of this row
-    float mx = fmaxf(l, __shfl_xor_sync(full, l, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(full, mx, 2));
-    const float e = comb_lane ? expf(l - mx) : 1.f;
-    const float e0 = __shfl_sync(full, e, rb), e1 = __shfl_sync(full, e, rb + 1);
-    const float e2 = __shfl_sync(full, e, rb + 2), e3 = __shfl_sync(full, e, rb + 3);
-    const float inv = __frcp_rn(((e0 + e1) + e2) + e3);
+    reinterpret_cast<float4 *>(pre_out)[t] = make_float4(pp[0], pp[1], pp[2], pp[3]);
+    reinterpret_cast<float4 *>(post_out)[t] = make_float4(po[0], po[1], po[2], po[3]);
     const float eps = c.sinkhorn_eps;
-    float x = fmaf(e, inv, eps);
-    // column normalisation: (c0k + c1k) + (c2k + c3k), plus eps
-    float cs = x + __shfl_xor_sync(full, x, 4);
-    cs = cs + __shfl_xor_sync(full, cs, 8);
-    x = x * __frcp_rn(cs + eps);
-    for (int it = 1; it < c.sinkhorn_iters; ++it) {
-        const float c0 = __shfl_sync(full, x, rb), c1 = __shfl_sync(full, x, rb + 1);
-        const float c2 = __shfl_sync(full, x, rb + 2), c3 = __shfl_sync(full, x, rb + 3);
-        x = x * __frcp_rn((((c0 + c1) + c2) + c3) + eps);
-        cs = x + __shfl_xor_sync(full, x, 4);
-        cs = cs + __shfl_xor_sync(full, cs, 8);
-        x = x * __frcp_rn(cs + eps);
+    float x[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        float l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            l[k] = fmaf(v[(8 + 4 * r + k) * stride] * rstd, s2, __ldg(c.base + 8 + 4 * r + k));
+        const float mx = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
+        float e[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) e[k] = expf(l[k] - mx);
+        const float inv = rcp_nr(((e[0] + e[1]) + e[2]) + e[3]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[r][k] = fmaf(e[k], inv, eps);
     }
-    if (comb_lane) comb_out[t * 16 + (lane - 16)] = x;
-    return pre;
+    auto col_normalize = [&]() {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float r = rcp_nr(((x[0][k] + x[1][k]) + (x[2][k] + x[3][k])) + eps);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i][k] = x[i][k] * r;
+        }
+    };
+    col_normalize();
+    for (int it = 1; it < c.sinkhorn_iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float r = rcp_nr((((x[i][0] + x[i][1]) + x[i][2]) + x[i][3]) + eps);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) x[i][k] = x[i][k] * r;
+        }
+        col_normalize();
+    }
+    float4 *cb = reinterpret_cast<float4 *>(comb_out) + t * 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) cb[i] = make_float4(x[i][0], x[i][1], x[i][2], x[i][3]);
 }
 
 // out = bf16((li * rstd_li) * norm_w) for 8 values

@@ -141,12 +141,13 @@ void plan(long long T, int H, int *n_slices, int *slice_w) {
     *slice_w = best_d * kChunk;
 }
 
-// Workspace: per-slice partials [S][T][28] fp32, then (each 256-byte
+// Workspace: per-item partials [tiles][S][25][128] fp32, then (each 256-byte
 // aligned) the shifted form's per-slice collapse sums [S][T] fp32 and its
 // publication flags [tiles][S][4] u64.
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 size_t partials_bytes(long long T, int S) {
-    return align256(static_cast<size_t>(S) * static_cast<size_t>(T) * kPartStride * sizeof(float));
+    const size_t tiles = static_cast<size_t>((T + kTileT - 1) / kTileT);
+    return align256(tiles * static_cast<size_t>(S) * kPartVals * kTileT * sizeof(float));
 }
 size_t ssql_bytes(long long T, int S) {
     return align256(static_cast<size_t>(S) * static_cast<size_t>(T) * sizeof(float));
@@ -310,8 +311,9 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     fa.comb_out = comb_out;
     fa.T = T;
     fa.H = H;
-    if (mode == FUSED_SHIFTED) return cuda_status(launch_coefficients(fa, st));
-    return cuda_status(launch_finish_unshifted(fa, st));
+    if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
+    if (mode == FUSED_SHIFTED) return MHC_OK;
+    return cuda_status(launch_collapse_unshifted(fa, st));
 }
 
 }  // namespace
@@ -432,6 +434,18 @@ mhc_status mhc_debug_unarmed_wait(void *stream) {
     if (mhc_status s = current_device(&dev)) return s;
     return cuda_status(
         launch_unarmed_wait(dev->status, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
+}
+
+mhc_status mhc_debug_rcp_check(uint32_t first_bits, uint64_t count, unsigned long long *result,
+                               void *stream) {
+    if (!result) return MHC_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(result) & 7u) != 0) return MHC_ERR_ALIGN;
+    if (count == 0) return MHC_OK;
+    if (count > (1ull << 32) - first_bits) return MHC_ERR_SHAPE;
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    return cuda_status(launch_rcp_check(first_bits, count, result,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -18,7 +18,10 @@ constexpr int kXBytes = kTileT * kRowBytes;         // x / collapse tile
 constexpr int kWRows = 48;                          // 24 hi + 24 lo weight rows
 constexpr int kWBytes = 4 * kWRows * kRowBytes;     // weight tile of one chunk
 constexpr int kStageBytes = kResBytes + kXBytes + kWBytes;
-constexpr int kPartStride = 28;                     // floats per token per slice
+// Partials of one (tile, slice) item: value-major [kPartVals][kTileT] fp32,
+// values 0-23 the partial mixes (hi + lo), 24 the partial 4H sum of squares,
+// so that a warp reads or writes one value of 32 tokens as one 128-byte row.
+constexpr int kPartVals = 25;
 constexpr int kStreamThreads = 320;                 // TMA warp, MMA warp, 8 workers
 constexpr int kTmemCols = 64;
 
@@ -34,7 +37,7 @@ struct StreamArgs {
     const float *comb;       // [T,4,4]
     const float *pre_lag;    // [T,4] (shifted only)
     const uint8_t *weight;   // prepared tiles
-    float *partials;         // [n_slices][T][kPartStride]
+    float *partials;         // [tiles][n_slices][kPartVals][kTileT]
     unsigned int *status;    // device status word
     long long T;
     int H;
@@ -53,14 +56,14 @@ struct StreamArgs {
 };
 
 struct FinishArgs {
-    const float *partials;   // [n_slices][T][kPartStride]
+    const float *partials;   // [tiles][n_slices][kPartVals][kTileT]
     int n_slices;
     CoefArgs coef;
     const void *norm_w;      // [H] or NULL
     int nw_bf16;
     const uint16_t *cur;     // [T,4,H] stream the collapse reads (unshifted)
     uint16_t *layer_input;   // [T,H]
-    float *pre_out, *post_out, *comb_out;
+    float *pre_out, *post_out, *comb_out;   // the collapse reads pre_out
     long long T;
     int H;
 };
@@ -73,13 +76,15 @@ size_t stream_smem_bytes();
 cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x,
                           const CUtensorMap &rout, const StreamArgs &a, int n_slices, int n_items,
                           int grid, cudaStream_t s);
-cudaError_t launch_finish_unshifted(const FinishArgs &a, cudaStream_t s);
+cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s);
 cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *post,
                         const float *comb, uint16_t *out, long long T, int H, cudaStream_t s);
 cudaError_t launch_unarmed_wait(unsigned int *status, unsigned long long timeout_ns,
                                 cudaStream_t s);
+cudaError_t launch_rcp_check(uint32_t first, unsigned long long count, unsigned long long *out,
+                             cudaStream_t s);
 unsigned int *device_status_word();   // of the current device; NULL on failure
 
 }  // namespace mhc

@@ -274,6 +274,16 @@ __device__ __forceinline__ unsigned long long flag_acquire(const unsigned long l
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// Programmatic dependent launch: let the next kernel of the stream be
+// scheduled early / wait until the previous grid has completed and its
+// memory operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) {
     asm volatile("nanosleep.u32 %0;" ::"r"(ns));
 }
@@ -290,6 +300,11 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint4 &a, const uint
         : "memory");
 }
 // 16 bytes to global memory with an L2 policy; `p` 16-byte aligned.
+__device__ __forceinline__ void st_global_f32(float *p, float v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(p)), "f"(v), "l"(policy)
+                 : "memory");
+}
 __device__ __forceinline__ void st_global_v4(void *p, const uint4 &a, uint64_t policy) {
     asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
                  ::"l"(reinterpret_cast<uint64_t>(p)), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w),

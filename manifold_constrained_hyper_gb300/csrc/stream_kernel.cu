@@ -46,6 +46,7 @@ constexpr int kNumBars = 3 * kStages + 4 * kAccBufs + 3 + 1;
 constexpr int kSumsOff = kBarOff + 256;                // [buffers][2 halves][2 sums][128] fp32
 constexpr int kMiscOff = kSumsOff + kAccBufs * 2 * 2 * kTileT * 4;
 constexpr int kSmemUsed = kMiscOff + 64;
+static_assert(kSmemUsed + 1024 <= 227 * 1024, "shared memory per CTA");
 constexpr int kAccCols = 64;                           // one accumulator buffer (48 used)
 constexpr int kLiCol = kAccBufs * kAccCols;            // shifted: collapse buffers
 constexpr int kLiCols = 128;                           // 8 chunks x 16 columns
@@ -113,39 +114,6 @@ __device__ __forceinline__ uint4 collapse8(const uint4 (&cur)[4], const Coefs &c
         w[p] = bf2_pack_rn(acc);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// bf16((li * rstd_li) * w) for 8 values: two separately rounded products.
-__device__ __forceinline__ uint4 rmsnorm8(const uint32_t *li, float rstd_li, const float *w) {
-    uint32_t o[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const float lo = __fmul_rn(__fmul_rn(__uint_as_float(li[p] << 16), rstd_li), w[2 * p]);
-        const float hi =
-            __fmul_rn(__fmul_rn(__uint_as_float(li[p] & 0xFFFF0000u), rstd_li), w[2 * p + 1]);
-        o[p] = bf2_pack_rn(f2_pack(lo, hi));
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// 8 consecutive norm weights (fp32 or bf16 bits) as fp32.
-__device__ __forceinline__ void norm_w8(const void *nw, int bf16, long long h, float (&w)[8]) {
-    if (bf16) {
-        const uint4 a = ld_global_nc_v4(static_cast<const uint16_t *>(nw) + h);
-        const uint32_t ws[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            w[2 * i] = __uint_as_float(ws[i] << 16);
-            w[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
-        }
-    } else {
-        const float *p = static_cast<const float *>(nw) + h;
-        const uint4 a = ld_global_nc_v4(p), b = ld_global_nc_v4(p + 4);
-        w[0] = __uint_as_float(a.x); w[1] = __uint_as_float(a.y);
-        w[2] = __uint_as_float(a.z); w[3] = __uint_as_float(a.w);
-        w[4] = __uint_as_float(b.x); w[5] = __uint_as_float(b.y);
-        w[6] = __uint_as_float(b.z); w[7] = __uint_as_float(b.w);
-    }
 }
 
 __device__ __forceinline__ void regs_dec_producer() {
@@ -241,6 +209,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         tma_prefetch_desc(&tm_res);
         if (MODE != PRE_ONLY) { tma_prefetch_desc(&tm_x); tma_prefetch_desc(&tm_rout); }
     }
+    // the finishing kernel launched after this one may start its blocks as
+    // soon as SMs free up; it waits for this grid's completion itself
+    if (tid == 0) griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -469,6 +440,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         const int t = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint64_t pol_out = policy_evict_first();
+        const uint64_t pol_keep = policy_evict_last();
         // Item k is published as soon as its accumulator is ready; its layer
         // input is written one item later, once the tile's other slices have
         // published too (by then they almost always have).
@@ -500,20 +472,15 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 }
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok && gt < a.T) {
-                    float out[kPartStride];
+                    // value-major partials of the item, kept in L2 for the
+                    // kernel that reduces them next: a warp writes 128-byte rows
+                    float *dst = a.partials +
+                                 (static_cast<size_t>(it.tile) * n_slices + it.slice) * kPartVals * kTileT + t;
 #pragma unroll
                     for (int i = 0; i < 24; ++i)
-                        out[i] = __uint_as_float(v[i]) + __uint_as_float(v[24 + i]);
-                    out[24] = ssq;
-                    out[25] = ssql;
-                    out[26] = 0.f;
-                    out[27] = 0.f;
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        a.partials + (static_cast<size_t>(it.slice) * a.T + gt) * kPartStride);
-#pragma unroll
-                    for (int i = 0; i < kPartStride / 4; ++i)
-                        dst[i] = make_float4(out[4 * i], out[4 * i + 1], out[4 * i + 2],
-                                             out[4 * i + 3]);
+                        st_global_f32(dst + i * kTileT,
+                                      __uint_as_float(v[i]) + __uint_as_float(v[24 + i]), pol_keep);
+                    st_global_f32(dst + 24 * kTileT, ssq, pol_keep);
                     if (MODE == FUSED_SHIFTED)
                         a.ssql[static_cast<size_t>(it.slice) * a.T + gt] = ssql;
                 }
@@ -532,7 +499,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             const int kn = k - 1, lb = kn % kLiBufs;
             const Item it = item_of(kn, n_slices);
             const long long gt = static_cast<long long>(it.tile) * kTileT + t;
-            bool ok = !*abort_flag;
+            bool ok = __all_sync(0xffffffffu, !*abort_flag);
             // every slice of the tile published: rstd of each token's collapse
             if (ok && a.norm_w != nullptr) {
                 const unsigned long long *fl = a.flags + static_cast<long long>(it.tile) * n_slices * 4;

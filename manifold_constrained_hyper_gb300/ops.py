@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "MHC_OK", 1: "MHC_ERR_NULL", 2: "MHC_ERR_ALIGN", 3: "MHC_ERR_
 EXPORTS = ("mhc_weight_bytes", "mhc_prepare_weight", "mhc_post", "mhc_workspace_bytes",
            "mhc_pre", "mhc_boundary_fused", "mhc_get_device_status", "mhc_last_timeout_site",
            "mhc_status_string", "mhc_set_wait_timeout_ns", "mhc_debug_unarmed_wait",
-           "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc")
+           "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc",
+           "mhc_debug_rcp_check")
 
 
 class MhcError(RuntimeError):
@@ -86,6 +87,7 @@ def load():
         "mhc_set_wait_timeout_ns": (None, [ctypes.c_uint64]),
         "mhc_debug_unarmed_wait": (i32, [P]),
         "mhc_debug_record_between": (None, [P]),
+        "mhc_debug_rcp_check": (i32, [ctypes.c_uint32, ctypes.c_uint64, P, P]),
         "mhc_plan": (i32, [i64, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -262,6 +264,20 @@ def mhc_set_wait_timeout_ns(ns: int):
 
 def mhc_debug_unarmed_wait(stream=None):
     _check(load().mhc_debug_unarmed_wait(_stream(stream)), "mhc_debug_unarmed_wait")
+
+
+def mhc_debug_rcp_check(first_bits: int, count: int, stream=None):
+    """(number of bit patterns in [first_bits, first_bits + count) whose
+    library reciprocal differs from the correctly rounded one, smallest such
+    pattern or None)."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    res = torch.tensor([0, -1], dtype=torch.int64, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())
+    _check(load().mhc_debug_rcp_check(first_bits, count, ctypes.c_void_p(res.data_ptr()),
+                                      _stream(s)), "mhc_debug_rcp_check")
+    s.synchronize()
+    n, first = (int(v) for v in res.cpu().tolist())
+    return n, (None if n == 0 else first & 0xFFFFFFFF)
 
 
 def mhc_debug_record_between(event):

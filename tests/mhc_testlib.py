@@ -41,7 +41,7 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
             weight=None, in_place: bool = False, dev_tensors: dict | None = None):
     """Runs one boundary call on the GPU. `d` holds numpy inputs (synth);
     `dev_tensors` may carry residual/x already on the device. Returns a dict
-    of numpy outputs plus the workspace partials [S][T][28]."""
+    of numpy outputs plus the workspace partials as [S][T][25]."""
     dev_tensors = dev_tensors or {}
     res = dev_tensors.get("residual")
     if res is None:
@@ -72,7 +72,11 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
     torch.cuda.synchronize()
     assert ops.mhc_get_device_status() == 0
     S, _ = ops.plan(T, H)
-    part = ws[: S * T * 28 * 4].view(torch.float32).view(S, T, 28).cpu().numpy()
+    # the library's internal partials: per (128-token tile, slice) item, 25
+    # value-major rows of 128 tokens (24 mixes, then the 4H sum of squares)
+    tiles = (T + 127) // 128
+    part = (ws[: tiles * S * 25 * 128 * 4].view(torch.float32).view(tiles, S, 25, 128)
+            .permute(1, 0, 3, 2).reshape(S, tiles * 128, 25)[:, :T, :].cpu().numpy())
     out.update(layer_input_dev=li, pre=pr.cpu().numpy(), post=po.cpu().numpy(),
                comb=cb.cpu().numpy(), partials=part)
     return out

@@ -46,7 +46,7 @@ def test_sizes_and_plan(lib):
     for T, H in [(1, 256), (64, 7168), (512, 7168), (8192, 7168), (1024, 4096), (5, 32)]:
         S, w = ops.plan(T, H)
         assert S * w == H and w % 32 == 0
-        assert ops.workspace_bytes(T, H) >= S * T * 28 * 4
+        assert ops.workspace_bytes(T, H) >= S * ((T + 127) // 128) * 25 * 128 * 4
     assert ops.plan(8192, 7168) == (28, 256)
 
 
@@ -84,3 +84,8 @@ def test_argument_errors_before_any_device_work(lib):
                                   _P(A * 6), _P(A * 7), None, 0, ctypes.byref(p), 4, 256,
                                   _P(A * 8), _P(A * 9), _P(A * 10), _P(A * 11), _P(A * 12),
                                   _P(A * 13), 1 << 20, None) == 1
+    # reciprocal check hook: NULL / misaligned result, range past 2^32
+    assert lib.mhc_debug_rcp_check(0, 16, None, None) == 1
+    assert lib.mhc_debug_rcp_check(0, 16, _P(A + 4), None) == 2
+    assert lib.mhc_debug_rcp_check(0xFFFFFFF0, 17, _P(A), None) == 3
+    assert lib.mhc_debug_rcp_check(0, 0, _P(A), None) == 0

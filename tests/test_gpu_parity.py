@@ -220,6 +220,21 @@ def test_prefill_t8192_h7168_sampled_tokens():
     compare("shifted", gsel, o)
 
 
+# ------------------------------------------------------------------ reciprocal
+
+
+def test_coefficient_reciprocal_is_correctly_rounded_for_every_normal_input():
+    """The coefficients divide through the "mhc_boundary" page's rcp (hardware
+    approximation plus one Newton-Raphson step), the oracle through an IEEE
+    division. Exhaustively, for every positive normal x whose reciprocal is
+    normal (2^-126 <= x <= 2^126: sums of Sinkhorn rows and columns, softmax
+    sums, sigmoid denominators clamped at 2^126), the two are the same
+    float."""
+    lo, hi = 0x00800000, 0x7E800000
+    n, first = ops.mhc_debug_rcp_check(lo, hi - lo + 1)
+    assert n == 0, f"{n} patterns differ, first {first:#010x}"
+
+
 # ------------------------------------------------------------------ bounded waits
 
 
