@@ -57,6 +57,12 @@ def alg_bytes_stream_kernel(T: int, H: int) -> int:
     return T * (20 * H + 96) + 384 * H
 
 
+# DRAM bytes (read + write) of one streaming-kernel launch of the 8192 x 7168
+# workload, from one ncu capture of the current kernel
+# (profiles/boundary_prefill_t8192_h7168_dram.md). None for other sizes.
+STREAM_KERNEL_TRAFFIC = {(8192, 7168): 590.85e6 + 535.59e6}
+
+
 # ---------------------------------------------------------------- clocks
 
 
@@ -332,7 +338,7 @@ def run_ours(args):
         "achieved_frac_of_peak": gbps_call / peak,
         "kernel_ms": {"stream": stream_ms, "finish": finish_ms},
         "roofline": {"bound": "hbm", "kernel": "stream_kernel", "achieved": ach, "peak": peak,
-                     "unit": "GB/s", "frac": ach / peak, "traffic": None,
+                     "unit": "GB/s", "frac": ach / peak, "traffic": STREAM_KERNEL_TRAFFIC.get((T, H)),
                      "peak_source": peak_kind},
         "cpu_baseline": cpu,
         "e2e": e2e,
