@@ -112,15 +112,17 @@ constexpr int kCoefThreads = kPartVals * 32;
 
 __global__ void __launch_bounds__(kCoefThreads, 2) coefficients_kernel(const FinishArgs a) {
     __shared__ float red[kPartVals][kCoefTokens];
+    __shared__ float consts[32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    stage_coef_consts(a.coef, consts, threadIdx.x);
     const long long t0 = static_cast<long long>(blockIdx.x) * kCoefTokens;
     const long long t = t0 + lane;
     const long long tile = t0 / kTileT;
     const int tin = static_cast<int>(t0 % kTileT) + lane;
     griddep_wait();
     if (t < a.T) {
-        const float *p = a.partials + (tile * a.n_slices * kPartVals + warp) * kTileT + tin;
-        const long long step = static_cast<long long>(kPartVals) * kTileT;
+        const float *p = a.partials + tile * a.n_slices * kItemFloats + warp * kTileT + tin;
+        const long long step = kItemFloats;
         float v = 0.f;
         for (int s = 0; s < a.n_slices; s += 32) {
             float w[32];
@@ -134,8 +136,8 @@ __global__ void __launch_bounds__(kCoefThreads, 2) coefficients_kernel(const Fin
     }
     __syncthreads();
     if (warp == 0 && t < a.T)
-        coefficients_thread(&red[0][lane], kCoefTokens, a.coef, a.H, t, a.pre_out, a.post_out,
-                            a.comb_out);
+        coefficients_thread(&red[0][lane], kCoefTokens, consts, a.coef, a.H, t, a.pre_out,
+                            a.post_out, a.comb_out);
 }
 
 // ------------------------------------------------------------ collapse (unshifted)

@@ -31,19 +31,20 @@ static __device__ __forceinline__ float sigmoid_clamped(float v) {
 // the reciprocal of the row sum, plus eps), one column normalisation, then
 // iters - 1 times a row and a column normalisation; column sums pair rows
 // (0, 1) and (2, 3).
+// sb: scale[0..2] then base[0..23], staged in shared memory by the caller.
 static __device__ __forceinline__ void coefficients_thread(const float *v, int stride,
-                                                           const CoefArgs &c, int H, long long t,
-                                                           float *pre_out, float *post_out,
-                                                           float *comb_out) {
+                                                           const float *sb, const CoefArgs &c,
+                                                           int H, long long t, float *pre_out,
+                                                           float *post_out, float *comb_out) {
     const float rstd =
         rsqrtf(__fdiv_rn(v[24 * stride], static_cast<float>(4 * H)) + c.hc_norm_eps);
-    const float s0 = __ldg(c.scale + 0), s1 = __ldg(c.scale + 1), s2 = __ldg(c.scale + 2);
+    const float s0 = sb[0], s1 = sb[1], s2 = sb[2];
+    const float *bs = sb + 3;
     float pp[4], po[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        pp[i] = sigmoid_clamped(fmaf(v[i * stride] * rstd, s0, __ldg(c.base + i))) + c.hc_pre_eps;
-        po[i] = sigmoid_clamped(fmaf(v[(4 + i) * stride] * rstd, s1, __ldg(c.base + 4 + i))) *
-                c.hc_post_mult;
+        pp[i] = sigmoid_clamped(fmaf(v[i * stride] * rstd, s0, bs[i])) + c.hc_pre_eps;
+        po[i] = sigmoid_clamped(fmaf(v[(4 + i) * stride] * rstd, s1, bs[4 + i])) * c.hc_post_mult;
     }
     reinterpret_cast<float4 *>(pre_out)[t] = make_float4(pp[0], pp[1], pp[2], pp[3]);
     reinterpret_cast<float4 *>(post_out)[t] = make_float4(po[0], po[1], po[2], po[3]);
@@ -54,7 +55,7 @@ static __device__ __forceinline__ void coefficients_thread(const float *v, int s
         float l[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            l[k] = fmaf(v[(8 + 4 * r + k) * stride] * rstd, s2, __ldg(c.base + 8 + 4 * r + k));
+            l[k] = fmaf(v[(8 + 4 * r + k) * stride] * rstd, s2, bs[8 + 4 * r + k]);
         const float mx = fmaxf(fmaxf(l[0], l[1]), fmaxf(l[2], l[3]));
         float e[4];
 #pragma unroll
@@ -84,6 +85,12 @@ static __device__ __forceinline__ void coefficients_thread(const float *v, int s
     float4 *cb = reinterpret_cast<float4 *>(comb_out) + t * 4;
 #pragma unroll
     for (int i = 0; i < 4; ++i) cb[i] = make_float4(x[i][0], x[i][1], x[i][2], x[i][3]);
+}
+
+// Stages scale[0..2] and base[0..23] into sb[0..26] (threads 0..26 of the caller's group).
+static __device__ __forceinline__ void stage_coef_consts(const CoefArgs &c, float *sb, int i) {
+    if (i < 3) sb[i] = __ldg(c.scale + i);
+    else if (i < 27) sb[i] = __ldg(c.base + i - 3);
 }
 
 // out = bf16((li * rstd_li) * norm_w) for 8 values

@@ -141,13 +141,13 @@ void plan(long long T, int H, int *n_slices, int *slice_w) {
     *slice_w = best_d * kChunk;
 }
 
-// Workspace: per-item partials [tiles][S][25][128] fp32, then (each 256-byte
+// Workspace: per-item partial blocks [tiles][S] of 128 x 28 fp32, then (each 256-byte
 // aligned) the shifted form's per-slice collapse sums [S][T] fp32 and its
 // publication flags [tiles][S][4] u64.
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 size_t partials_bytes(long long T, int S) {
     const size_t tiles = static_cast<size_t>((T + kTileT - 1) / kTileT);
-    return align256(tiles * static_cast<size_t>(S) * kPartVals * kTileT * sizeof(float));
+    return align256(tiles * static_cast<size_t>(S) * kItemFloats * sizeof(float));
 }
 size_t ssql_bytes(long long T, int S) {
     return align256(static_cast<size_t>(S) * static_cast<size_t>(T) * sizeof(float));
@@ -289,6 +289,9 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // the shifted form finishes in-kernel: every slice of a tile must be in
     // flight at once, and an item's collapse must fit its TMEM buffer
     if (mode == FUSED_SHIFTED && (S > grid || w / kChunk > 8)) return MHC_ERR_UNSUPPORTED;
+    // a single wave of items: the shifted form's finishers form the
+    // coefficients too (no second kernel)
+    sa.fuse_coef = mode == FUSED_SHIFTED && items <= grid;
     if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, sa, S,
                                                  static_cast<int>(items), grid, st)))
         return s;
@@ -311,6 +314,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     fa.comb_out = comb_out;
     fa.T = T;
     fa.H = H;
+    if (sa.fuse_coef) return MHC_OK;
     if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
     if (mode == FUSED_SHIFTED) return MHC_OK;
     return cuda_status(launch_collapse_unshifted(fa, st));

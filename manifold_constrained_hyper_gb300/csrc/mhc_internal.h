@@ -18,10 +18,15 @@ constexpr int kXBytes = kTileT * kRowBytes;         // x / collapse tile
 constexpr int kWRows = 48;                          // 24 hi + 24 lo weight rows
 constexpr int kWBytes = 4 * kWRows * kRowBytes;     // weight tile of one chunk
 constexpr int kStageBytes = kResBytes + kXBytes + kWBytes;
-// Partials of one (tile, slice) item: value-major [kPartVals][kTileT] fp32,
-// values 0-23 the partial mixes (hi + lo), 24 the partial 4H sum of squares,
-// so that a warp reads or writes one value of 32 tokens as one 128-byte row.
+// Partials of one (tile, slice) item, a block of kItemFloats fp32: per token,
+// values 0-23 the partial mixes (hi + lo), 24 the partial 4H sum of squares.
+// Value-major [kPartVals][kTileT] (a warp reads or writes one value of 32
+// tokens as one 128-byte row) when a separate kernel reduces them;
+// token-major [kTileT][kTokStride] (16-byte aligned runs) when the streaming
+// kernel's finishers reduce them for a few tokens each (a single wave).
 constexpr int kPartVals = 25;
+constexpr int kTokStride = 28;
+constexpr int kItemFloats = kTileT * kTokStride;
 constexpr int kStreamThreads = 320;                 // TMA warp, MMA warp, 8 workers
 constexpr int kTmemCols = 64;
 
@@ -37,7 +42,7 @@ struct StreamArgs {
     const float *comb;       // [T,4,4]
     const float *pre_lag;    // [T,4] (shifted only)
     const uint8_t *weight;   // prepared tiles
-    float *partials;         // [tiles][n_slices][kPartVals][kTileT]
+    float *partials;         // [tiles][n_slices] item blocks of kItemFloats
     unsigned int *status;    // device status word
     long long T;
     int H;
@@ -53,10 +58,11 @@ struct StreamArgs {
     int out32;                   // layer_input 32-byte aligned
     uint16_t *layer_input;       // [T,H]
     float *pre_out, *post_out, *comb_out;
+    int fuse_coef;               // one item per CTA: the finishers also form the coefficients
 };
 
 struct FinishArgs {
-    const float *partials;   // [tiles][n_slices][kPartVals][kTileT]
+    const float *partials;   // [tiles][n_slices] value-major item blocks of kItemFloats
     int n_slices;
     CoefArgs coef;
     const void *norm_w;      // [H] or NULL

@@ -274,6 +274,21 @@ __device__ __forceinline__ unsigned long long flag_acquire(const unsigned long l
     asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// Relaxed flag read (several may be in flight); a fence_acq_rel_gpu after the
+// reads that saw the released values makes the data behind them visible.
+__device__ __forceinline__ unsigned long long flag_relaxed(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+// bar.sync on a named barrier shared by `threads` threads (whole, converged warps).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    __syncwarp();
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 // Programmatic dependent launch: let the next kernel of the stream be
 // scheduled early / wait until the previous grid has completed and its
 // memory operations are visible.

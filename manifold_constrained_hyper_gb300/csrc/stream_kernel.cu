@@ -21,8 +21,9 @@
 // workers also collapse the updated residual with the lagged pre into TMEM;
 // the finishers publish the item with a per-call flag, wait until every
 // slice of the tile has published, and write the layer input
-// bf16((li * rsqrt(sum li^2 / H + eps)) * norm_w) from TMEM. A small kernel
-// forms the coefficients from the partials afterwards.
+// bf16((li * rsqrt(sum li^2 / H + eps)) * norm_w) from TMEM. When every CTA
+// has a single item (a decode batch) the finishers then also form the
+// coefficients; otherwise a small kernel forms them from the partials.
 //
 // Warps: 0 TMA producer and TMEM owner, 1 MMA issuer, 2-3 idle, 4-11
 // workers (token 32*(warp%4) + lane, so a warp's tokens are its TMEM lane
@@ -45,7 +46,12 @@ constexpr int kLiBufs = 3;                             // shifted: collapse buff
 constexpr int kNumBars = 3 * kStages + 4 * kAccBufs + 3 + 1;
 constexpr int kSumsOff = kBarOff + 256;                // [buffers][2 halves][2 sums][128] fp32
 constexpr int kMiscOff = kSumsOff + kAccBufs * 2 * 2 * kTileT * 4;
-constexpr int kSmemUsed = kMiscOff + 64;
+constexpr int kRedOff = kMiscOff + 64;                 // finisher scratch: [3][128] + [32] fp32
+constexpr int kRoundTok = 5;                           // tokens per coefficient round (<= 128 / 25)
+constexpr int kFinThreads = 128;
+constexpr int kFinBarrier = 1;                         // named barrier of the finisher warps
+constexpr int kSmemUsed = kRedOff + (3 * kFinThreads + 32) * 4;
+static_assert(kRoundTok * kPartVals <= kFinThreads, "one pair per finisher thread");
 static_assert(kSmemUsed + 1024 <= 227 * 1024, "shared memory per CTA");
 constexpr int kAccCols = 64;                           // one accumulator buffer (48 used)
 constexpr int kLiCol = kAccBufs * kAccCols;            // shifted: collapse buffers
@@ -437,6 +443,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // ---------------------------------------------------- finishers
         regs_dec_finisher();
         const int q = warp & 3;
+        float *red = reinterpret_cast<float *>(gbase + kRedOff);
+        float *rsum = red + 2 * kFinThreads;
+        float *consts = red + 3 * kFinThreads;
+        stage_coef_consts(a.coef, consts, tid - 12 * 32);
+        named_barrier_sync(kFinBarrier, kFinThreads);
         const int t = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint64_t pol_out = policy_evict_first();
@@ -472,25 +483,46 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 }
                 ok = __all_sync(0xffffffffu, ok);
                 if (ok && gt < a.T) {
-                    // value-major partials of the item, kept in L2 for the
-                    // kernel that reduces them next: a warp writes 128-byte rows
-                    float *dst = a.partials +
-                                 (static_cast<size_t>(it.tile) * n_slices + it.slice) * kPartVals * kTileT + t;
+                    float *rec = a.partials +
+                                 (static_cast<size_t>(it.tile) * n_slices + it.slice) * kItemFloats;
+                    if (a.fuse_coef) {
+                        // token-major [128][28]: the finishers of this kernel
+                        // read a token's 25 values as one contiguous run
+                        float4 *dst = reinterpret_cast<float4 *>(rec + t * kTokStride);
+                        float o[kTokStride];
 #pragma unroll
-                    for (int i = 0; i < 24; ++i)
-                        st_global_f32(dst + i * kTileT,
-                                      __uint_as_float(v[i]) + __uint_as_float(v[24 + i]), pol_keep);
-                    st_global_f32(dst + 24 * kTileT, ssq, pol_keep);
+                        for (int i = 0; i < 24; ++i) o[i] = __uint_as_float(v[i]) + __uint_as_float(v[24 + i]);
+                        o[24] = ssq;
+                        o[25] = o[26] = o[27] = 0.f;
+#pragma unroll
+                        for (int i = 0; i < kTokStride / 4; ++i)
+                            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    } else {
+                        // value-major [25][128], kept in L2 for the kernel that
+                        // reduces them next: a warp writes 128-byte rows
+                        float *dst = rec + t;
+#pragma unroll
+                        for (int i = 0; i < 24; ++i)
+                            st_global_f32(dst + i * kTileT,
+                                          __uint_as_float(v[i]) + __uint_as_float(v[24 + i]), pol_keep);
+                        st_global_f32(dst + 24 * kTileT, ssq, pol_keep);
+                    }
                     if (MODE == FUSED_SHIFTED)
                         a.ssql[static_cast<size_t>(it.slice) * a.T + gt] = ssql;
                 }
                 // publish this quarter of the item to the tile's other slices
+                // (a single wave: the whole item at once, after the four
+                // finisher warps have written, with one flag)
                 if (MODE == FUSED_SHIFTED) {
-                    __syncwarp();
-                    if (lane == 0)
-                        flag_release(a.flags +
-                                         (static_cast<long long>(it.tile) * n_slices + it.slice) * 4 + q,
-                                     a.epoch);
+                    unsigned long long *flag =
+                        a.flags + (static_cast<long long>(it.tile) * n_slices + it.slice) * 4;
+                    if (a.fuse_coef) {
+                        named_barrier_sync(kFinBarrier, kFinThreads);
+                        if (q == 0 && lane == 0) flag_release(flag, a.epoch);
+                    } else {
+                        __syncwarp();
+                        if (lane == 0) flag_release(flag + q, a.epoch);
+                    }
                 }
             }
             if (MODE != FUSED_SHIFTED || k == 0) continue;
@@ -500,39 +532,94 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             const Item it = item_of(kn, n_slices);
             const long long gt = static_cast<long long>(it.tile) * kTileT + t;
             bool ok = __all_sync(0xffffffffu, !*abort_flag);
-            // every slice of the tile published: rstd of each token's collapse
-            if (ok && a.norm_w != nullptr) {
+            // every slice of the tile published. The layer RMSNorm needs the
+            // flags of this warp's token quarter only: one acquire read per
+            // slice, spread over the lanes. Forming the coefficients here
+            // needs every quarter's flags: relaxed reads, all in flight, then
+            // one acquire fence once the warp has seen them all.
+            if (ok && (a.norm_w != nullptr || a.fuse_coef)) {
                 const unsigned long long *fl = a.flags + static_cast<long long>(it.tile) * n_slices * 4;
+                const int nf = n_slices;
                 uint64_t t_start = 0;
-                for (int f = lane; f < n_slices * 4 && ok; f += 32) {
-                    while (flag_acquire(fl + f) != a.epoch) {
-                        if (*abort_flag) { ok = false; break; }
-                        const uint64_t now = globaltimer_ns();
-                        if (t_start == 0) {
-                            t_start = now;
-                        } else if (now - t_start > tmo) {
+                while (true) {
+                    bool seen = true;
+                    if (a.fuse_coef) {
+                        for (int f0 = lane; f0 < nf; f0 += 32 * 8) {
+                            unsigned long long v[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                v[i] = f0 + 32 * i < nf ? flag_relaxed(fl + 4 * (f0 + 32 * i)) : a.epoch;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) seen = seen && v[i] == a.epoch;
+                        }
+                    } else {
+                        for (int f = lane; f < nf; f += 32)
+                            seen = seen && flag_acquire(fl + 4 * f + q) == a.epoch;
+                    }
+                    if (__all_sync(0xffffffffu, seen)) break;
+                    if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+                    // lane 0's clock, so that the whole warp takes the same branch
+                    const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+                    if (t_start == 0) {
+                        t_start = now;
+                    } else if (now - t_start > tmo) {
+                        if (lane == 0) {
                             record_failure(a.status, 7, SITE_TILE_FLAGS);
                             *abort_flag = 1;
-                            ok = false;
-                            break;
                         }
-                        nanosleep_ns(256);
+                        ok = false;
+                        break;
                     }
+                    nanosleep_ns(a.fuse_coef ? 64 : 256);
                 }
-                ok = __all_sync(0xffffffffu, ok);
+                if (a.fuse_coef) fence_acq_rel_gpu();
+                __syncwarp();
             }
             float rstd_li = 0.f;
-            if (ok && gt < a.T && a.norm_w != nullptr) {
+            if (a.fuse_coef) {
+                // single wave: the four finisher warps share the reduction. The
+                // tile's valid tokens form ntg groups of 32; each group's
+                // slices are cut into G = 4 / ntg consecutive ranges; warp w
+                // sums token group w % ntg over range w / ntg in slice order,
+                // and each token adds its G range sums in range order.
+                const long long tv = a.T - static_cast<long long>(it.tile) * kTileT;
+                const int ntg = tv >= kTileT ? 4 : static_cast<int>((tv + 31) / 32);
+                const int G = 4 / ntg;
+                const int tg = q % ntg, sg = q / ntg;
+                const long long gtok = static_cast<long long>(it.tile) * kTileT + tg * 32 + lane;
+                float part = 0.f;
+                if (ok && a.norm_w != nullptr && sg < G && gtok < a.T) {
+                    const int per = (n_slices + G - 1) / G;
+                    const int s_end = (sg + 1) * per < n_slices ? (sg + 1) * per : n_slices;
+                    const float *pp = a.ssql + gtok;
+                    const size_t step = static_cast<size_t>(a.T);
+                    for (int s2 = sg * per; s2 < s_end; s2 += 32) {
+                        float vv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) vv[i] = s2 + i < s_end ? pp[(s2 + i) * step] : 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (s2 + i < s_end) part += vv[i];
+                    }
+                }
+                rsum[q * 32 + lane] = part;
+                named_barrier_sync(kFinBarrier, kFinThreads);
+                if (ok && gt < a.T && a.norm_w != nullptr) {
+                    float sl = 0.f;
+                    for (int g = 0; g < G; ++g) sl += rsum[(g * ntg + q) * 32 + lane];
+                    rstd_li = rsqrtf(__fdiv_rn(sl, static_cast<float>(a.H)) + a.coef.norm_eps);
+                }
+            } else if (ok && gt < a.T && a.norm_w != nullptr) {
                 // independent loads, added in slice order
                 const float *pp = a.ssql + gt;
                 const size_t step = static_cast<size_t>(a.T);
                 float sl = 0.f;
-                for (int s2 = 0; s2 < n_slices; s2 += 16) {
-                    float vv[16];
+                for (int s2 = 0; s2 < n_slices; s2 += 32) {
+                    float vv[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) vv[i] = s2 + i < n_slices ? pp[(s2 + i) * step] : 0.f;
+                    for (int i = 0; i < 32; ++i) vv[i] = s2 + i < n_slices ? pp[(s2 + i) * step] : 0.f;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
+                    for (int i = 0; i < 32; ++i)
                         if (s2 + i < n_slices) sl += vv[i];
                 }
                 rstd_li = rsqrtf(__fdiv_rn(sl, static_cast<float>(a.H)) + a.coef.norm_eps);
@@ -592,6 +679,63 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(li_empty(lb));
+
+            // ---- one item per CTA (a single wave): the item also forms the
+            // coefficients of the tile's tokens slice + S * j. In rounds of up
+            // to kRoundTok tokens, the 128 finisher threads split the (token,
+            // value) pairs and, when there are fewer than 128 pairs, the slices
+            // into G consecutive groups; each thread sums its group in slice
+            // order (loads through L2 only: other CTAs wrote the partials in
+            // this kernel); one thread per pair adds the G group sums in group
+            // order; then one thread per token forms pre / post / comb. The
+            // rounds and barriers depend on the item only, so all four
+            // finisher warps take part.
+            if (a.fuse_coef) {
+                const int ntok = it.slice < kTileT ? (kTileT - 1 - it.slice) / n_slices + 1 : 0;
+                const long long gbase = static_cast<long long>(it.tile) * kTileT + it.slice;
+                const int ft = tid - 12 * 32;
+                for (int r0 = 0; r0 < ntok; r0 += kRoundTok) {
+                    int nr = ntok - r0 < kRoundTok ? ntok - r0 : kRoundTok;
+                    while (nr > 0 && gbase + static_cast<long long>(n_slices) * (r0 + nr - 1) >= a.T) --nr;
+                    const int pairs = nr * kPartVals;
+                    const int G = pairs > 0 ? kFinThreads / pairs : 1;
+                    const int per = (n_slices + G - 1) / G;
+                    if (ok && ft < pairs * G) {
+                        const int g = ft / pairs, pr = ft - g * pairs;
+                        const int j = pr / kPartVals, m = pr - j * kPartVals;
+                        const int tin = it.slice + n_slices * (r0 + j);
+                        const float *pp = a.partials + static_cast<size_t>(it.tile) * n_slices * kItemFloats +
+                                          tin * kTokStride + m;
+                        const size_t step = kItemFloats;
+                        const int s_end = (g + 1) * per < n_slices ? (g + 1) * per : n_slices;
+                        float sum = 0.f;
+                        for (int s2 = g * per; s2 < s_end; s2 += 32) {
+                            float vv[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) vv[i] = s2 + i < s_end ? __ldcg(pp + (s2 + i) * step) : 0.f;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (s2 + i < s_end) sum += vv[i];
+                        }
+                        red[ft] = sum;
+                    }
+                    named_barrier_sync(kFinBarrier, kFinThreads);
+                    // one thread per (token, value) adds the G range sums in order
+                    if (ok && ft < pairs) {
+                        float acc = 0.f;
+                        for (int g = 0; g < G; ++g) acc += red[g * pairs + ft];
+                        red[kFinThreads + ft] = acc;
+                    }
+                    named_barrier_sync(kFinBarrier, kFinThreads);
+                    if (ok && ft < nr) {
+                        const float *v = red + kFinThreads + ft * kPartVals;
+                        coefficients_thread(v, 1, consts, a.coef, a.H,
+                                            gbase + static_cast<long long>(n_slices) * (r0 + ft),
+                                            a.pre_out, a.post_out, a.comb_out);
+                    }
+                    named_barrier_sync(kFinBarrier, kFinThreads);
+                }
+            }
         }
         tc_fence_before();
         __syncwarp();

@@ -74,9 +74,17 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
     S, _ = ops.plan(T, H)
     # the library's internal partials: per (128-token tile, slice) item, 25
     # value-major rows of 128 tokens (24 mixes, then the 4H sum of squares)
+    # value-major [25][128] when a separate kernel reduces them; token-major
+    # [128][28] when the call is a single wave of items and the shifted
+    # streaming kernel reduces them itself
     tiles = (T + 127) // 128
-    part = (ws[: tiles * S * 25 * 128 * 4].view(torch.float32).view(tiles, S, 25, 128)
-            .permute(1, 0, 3, 2).reshape(S, tiles * 128, 25)[:, :T, :].cpu().numpy())
+    sms = min(152, torch.cuda.get_device_properties(0).multi_processor_count)
+    raw = ws[: tiles * S * 28 * 128 * 4].view(torch.float32).view(tiles, S, 28 * 128)
+    if mode == "shifted" and tiles * S <= sms:
+        blk = raw.view(tiles, S, 128, 28)[..., :25].permute(1, 0, 2, 3)
+    else:
+        blk = raw[..., : 25 * 128].reshape(tiles, S, 25, 128).permute(1, 0, 3, 2)
+    part = blk.reshape(S, tiles * 128, 25)[:, :T, :].cpu().numpy()
     out.update(layer_input_dev=li, pre=pr.cpu().numpy(), post=po.cpu().numpy(),
                comb=cb.cpu().numpy(), partials=part)
     return out
