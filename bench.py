@@ -59,8 +59,9 @@ def alg_bytes_stream_kernel(T: int, H: int) -> int:
 
 # DRAM bytes (read + write) of one streaming-kernel launch of the 8192 x 7168
 # workload, from one ncu capture of the current kernel
-# (profiles/boundary_prefill_t8192_h7168_dram.md). None for other sizes.
-STREAM_KERNEL_TRAFFIC = {(8192, 7168): 590.85e6 + 535.59e6}
+# (profiles/boundary_prefill_t8192_h7168_dram.md); empty until the capture of
+# the current kernel is taken. None for other sizes.
+STREAM_KERNEL_TRAFFIC = {(8192, 7168): 590.88e6 + 536.50e6}
 
 
 # ---------------------------------------------------------------- clocks
@@ -182,6 +183,91 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def measure_decode(dev, token_counts=None):
+    """Latency of one shifted call at the decode batch sizes, hidden H: per
+    call from a CUDA graph of 100 calls (launch cost amortised, L2 warm as in
+    a decode loop), eager per-call CUDA events with L2 warm, and eager with a
+    256 MB buffer written before each call (L2 cold). Inputs of each size
+    are the seeded decode workload (hidden 7168, seed 1000 + T)."""
+    import torch
+    from manifold_constrained_hyper_gb300 import ops, synth
+    token_counts = token_counts or synth.DECODE_TOKENS
+    H = synth.DECODE_HIDDEN
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)
+    out = {"hidden": H, "unit": "us/call", "graph": {}, "eager_warm": {}, "eager_cold_l2": {},
+           "slices": {}, "waves": {}}
+    sms = min(152, torch.cuda.get_device_properties(dev).multi_processor_count)
+    for T in token_counts:
+        cfg = synth.decode_workload(T)
+        d = synth.make_inputs(cfg["T"], cfg["H"], seed=cfg["seed"])
+        res, x = bf(d["residual"]), bf(d["x"])
+        post, comb, pl = f32(d["post"]), f32(d["comb"]), f32(d["pre_lag"])
+        scale, base, nw = f32(d["scale"]), f32(d["base"]), f32(d["norm_w"])
+        w = ops.mhc_prepare_weight(f32(d["fn"]))
+        outs = dict(residual_out=torch.empty_like(res),
+                    layer_input=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                    pre_out=torch.empty(T, 4, device=dev), post_out=torch.empty(T, 4, device=dev),
+                    comb_out=torch.empty(T, 4, 4, device=dev),
+                    workspace=torch.empty(ops.workspace_bytes(T, H), dtype=torch.uint8, device=dev))
+
+        def call():
+            ops.mhc_boundary_fused(x, res, post, comb, w, scale, base, nw, pl, **outs)
+
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(50)]
+        for a, b in ev:
+            a.record()
+            b.record()
+        torch.cuda.synchronize()
+        for a, b in ev:
+            a.record()
+            call()
+            b.record()
+        torch.cuda.synchronize()
+        warm = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+        cold = []
+        for a, b in ev[:20]:
+            scrub.add_(1)
+            a.record()
+            call()
+            b.record()
+            torch.cuda.synchronize()
+            cold.append(a.elapsed_time(b) * 1e3)
+        s = torch.cuda.Stream(device=dev)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            call()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(100):
+                    call()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        S, _ = ops.plan(T, H)
+        key = str(T)
+        out["graph"][key] = a.elapsed_time(b) * 1e3 / 100
+        out["eager_warm"][key] = warm
+        out["eager_cold_l2"][key] = statistics.median(cold)
+        out["slices"][key] = S
+        out["waves"][key] = -(-((T + 127) // 128 * S) // sms)
+        del g
+    if ops.mhc_get_device_status() != 0:
+        raise RuntimeError("device-side wait timed out during the decode sweep")
+    return out
 
 
 def run_ours(args):
@@ -323,6 +409,10 @@ def run_ours(args):
                "sample": f"{n} tokens of the {args.workload} distribution in {s:.1f} s, "
                          f"single-threaded C oracle, chunks of 32 tokens"}
 
+    decode = None
+    if not args.no_decode:
+        decode = measure_decode(dev)
+
     S, sw = ops.plan(T, H)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -343,6 +433,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": 2 * K,
+        "decode": decode,
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -361,6 +452,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-latency sweep (1-64 tokens)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-tokens", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=0,

@@ -186,6 +186,39 @@ bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T) {
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps of the last few calls of this host thread, by (kind, pointer,
+// H, T): a decode loop reuses its buffers, and encoding costs host time.
+struct MapCache {
+    struct Entry {
+        int kind = -1, H = 0;
+        long long T = 0;
+        const void *ptr = nullptr;
+        CUtensorMap map;
+    } e[6];
+    int next = 0;
+};
+thread_local MapCache t_maps;
+
+bool encode_cached(int kind, CUtensorMap *m, const void *ptr, int H, long long T) {
+    for (const auto &x : t_maps.e) {
+        if (x.kind == kind && x.ptr == ptr && x.H == H && x.T == T) {
+            *m = x.map;
+            return true;
+        }
+    }
+    const bool ok = kind == 0 ? encode_res(m, ptr, H, T) : encode_2d(m, ptr, H, T);
+    if (ok) {
+        auto &x = t_maps.e[t_maps.next];
+        t_maps.next = (t_maps.next + 1) % 6;
+        x.kind = kind;
+        x.ptr = ptr;
+        x.H = H;
+        x.T = T;
+        x.map = *m;
+    }
+    return ok;
+}
+
 mhc_status check_params(const mhc_params *p) {
     if (!p) return MHC_ERR_NULL;
     if (p->sinkhorn_iters < 1) return MHC_ERR_SHAPE;
@@ -251,10 +284,10 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     int S = 0, w = 0;
     plan(T, H, &S, &w);
     CUtensorMap m_res, m_x, m_rout;
-    if (!encode_res(&m_res, residual, H, T)) return MHC_ERR_CUDA;
+    if (!encode_cached(0, &m_res, residual, H, T)) return MHC_ERR_CUDA;
     m_x = m_rout = m_res;
     if (fused) {
-        if (!encode_2d(&m_x, x, H, T) || !encode_res(&m_rout, residual_out, H, T))
+        if (!encode_cached(1, &m_x, x, H, T) || !encode_cached(0, &m_rout, residual_out, H, T))
             return MHC_ERR_CUDA;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);

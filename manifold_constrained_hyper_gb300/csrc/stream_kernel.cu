@@ -31,6 +31,8 @@
 // finishers (token 32*(warp%4) + lane). Registers are redistributed per
 // warpgroup with setmaxnreg: 40 + 184 + 184 + 96 per thread, 64,512 of the
 // 65,536 the CTA is launched with.
+#include <atomic>
+
 #include "coef.cuh"
 #include "mhc_internal.h"
 #include "ptx.cuh"
@@ -748,8 +750,17 @@ cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtenso
                      const StreamArgs &a, int n_slices, int n_items, int grid, cudaStream_t s) {
     constexpr int smem = kSmemUsed + 1024;
     auto kern = stream_kernel<MODE>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // the shared-memory opt-in is per device: set it once for each
+    static std::atomic<unsigned long long> opted{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(opted.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        opted.fetch_or(bit, std::memory_order_release);
+    }
     if (MODE != FUSED_SHIFTED) {
         kern<<<grid, kThreads, smem, s>>>(res, x, rout, a, n_slices, n_items);
         return cudaGetLastError();

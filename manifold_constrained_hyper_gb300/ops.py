@@ -104,12 +104,13 @@ def _check(code: int, where: str):
 
 
 def _p(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # plain ints: the argtypes convert them (cheaper than c_void_p objects)
+    return None if t is None else t.data_ptr()
 
 
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 def _bf16(t: torch.Tensor, name: str):
