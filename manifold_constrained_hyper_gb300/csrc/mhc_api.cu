@@ -116,26 +116,35 @@ bool aliasing(const Range *outs, int no, const Range *ins, int ni, const void *m
 }
 
 // Hidden-slice plan: items of d chunks (d | H/32; a slice is d interleaved
-// 32-wide chunks) spread over kGridCap persistent CTAs; minimise the busiest
-// CTA's work, counting an item's partials (written and read back, ~0.35 of
-// a chunk's bytes) as cost. Items of at most 8 chunks keep enough CTAs on
-// one tile for DRAM row locality. A pure function of (T, H), so the
-// workspace size is too.
+// 32-wide chunks) spread over kGridCap persistent CTAs. At most kGridCap
+// slices, so that every slice of a tile can be in flight at once (the
+// shifted form's CTAs wait for one another). Among the item sizes of at most
+// 8 chunks (enough CTAs on one tile for DRAM row locality; the shifted
+// form's collapse buffer holds 8) minimise the busiest CTA's work, counting
+// kItemCost chunks' worth per item for its fixed costs (partials, the
+// finishers' waits and reductions). Only when no such size fits, take the
+// smallest larger one. A pure function of (T, H), so the workspace size is
+// too.
+constexpr double kItemCost = 2.0;
 void plan(long long T, int H, int *n_slices, int *slice_w) {
     const int chunks = H / kChunk;
     const long long tiles = (T + kTileT - 1) / kTileT;
     constexpr int kMaxItemChunks = 8;
     double best_cost = -1.0;
-    int best_d = 1;
+    int best_d = 0;
     for (int d = chunks < kMaxItemChunks ? chunks : kMaxItemChunks; d >= 1; --d) {
-        if (chunks % d) continue;
+        if (chunks % d || chunks / d > kGridCap) continue;
         const long long items = tiles * (chunks / d);
         const long long per_cta = (items + kGridCap - 1) / kGridCap;
-        const double cost = static_cast<double>(per_cta) * (d + 0.35);
+        const double cost = static_cast<double>(per_cta) * (d + kItemCost);
         if (best_cost < 0 || cost < best_cost - 1e-9) {
             best_cost = cost;
             best_d = d;
         }
+    }
+    if (best_d == 0) {
+        best_d = kMaxItemChunks + 1;
+        while (chunks % best_d || chunks / best_d > kGridCap) ++best_d;
     }
     *n_slices = chunks / best_d;
     *slice_w = best_d * kChunk;

@@ -48,6 +48,15 @@ def test_sizes_and_plan(lib):
         assert S * w == H and w % 32 == 0
         assert ops.workspace_bytes(T, H) >= S * ((T + 127) // 128) * 28 * 128 * 4
     assert ops.plan(8192, 7168) == (28, 256)
+    # every tile's slices fit in one wave of persistent CTAs; item sizes of at
+    # most 8 chunks wherever some such size fits
+    for H in range(32, 65537, 32):
+        for T in (1, 128, 129, 256, 512, 1024, 8192):
+            S, w = ops.plan(T, H)
+            assert S <= 152 and S * w == H, (T, H, S, w)
+            if H <= 152 * 8 * 32 and any((H // 32) % d == 0 and H // 32 // d <= 152
+                                         for d in range(1, 9)):
+                assert w <= 256, (T, H, S, w)
 
 
 def test_status_strings(lib):

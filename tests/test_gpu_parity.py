@@ -104,6 +104,19 @@ def test_ragged_tiles(mode, T, H):
     compare(mode, g, o, d=d)
 
 
+@pytest.mark.parametrize("mode", ["shifted", "unshifted", "pre"])
+@pytest.mark.parametrize("T", [256, 300, 1024])
+def test_slice_plans_at_hidden_7168(mode, T):
+    """Token counts whose plans differ at hidden 7168: 56 slices of 128 over
+    two tiles, 32 slices of 224 over three tiles with a ragged tail (both a
+    single wave: coefficients formed in the streaming kernel), and 32 slices
+    over eight tiles (two items per CTA: coefficients kernel)."""
+    d = synth.make_inputs(T, 7168, seed=500 + T)
+    g = run_gpu(mode, d)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, d=d)
+
+
 @pytest.mark.parametrize("mode", ["pre", "unshifted", "shifted"])
 def test_mid_batch_t512_h7168(mode):
     d = synth.workload_inputs("mid_t512_h7168")
