@@ -150,6 +150,27 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own shard of tokens (independent inputs)."""
+    return base_seed + 7919 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The job's time is its slowest rank's."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, tokens_per_rank: int, steps: int, ms: float) -> float:
+    """Tokens per second over all ranks (weak scaling: every rank has its own tokens)."""
+    return world * tokens_per_rank * steps / (ms / 1e3)
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -291,7 +312,7 @@ def run_ours(args):
         cfg["T"] = args.tokens
     T, H = cfg["T"], cfg["H"]
     extra = {k: v for k, v in cfg.items() if k not in ("T", "H", "seed")}
-    d = synth.make_inputs_device(T, H, cfg["seed"] + 7919 * rank, dev, **extra)
+    d = synth.make_inputs_device(T, H, rank_seed(cfg["seed"], rank), dev, **extra)
     f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
     res, x = d["residual_dev"], d["x_dev"]
     post, comb, pre_lag = f32(d["post"]), f32(d["comb"]), f32(d["pre_lag"])
@@ -343,15 +364,11 @@ def run_ours(args):
     status = ops.mhc_get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    total_ms = t_begin.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t_begin.elapsed_time(t_end), world, dev)
     stream_ms = statistics.mean(ev_s[i].elapsed_time(ev_m[i]) for i in range(K))
     finish_ms = statistics.mean(ev_m[i].elapsed_time(ev_e[i]) for i in range(K))
     ms_per_step = total_ms / K
-    value = world * T * K / (total_ms / 1e3)
+    value = whole_job_rate(world, T, K, total_ms)
     peak, peak_kind = measured_peaks()
     gbps_call = alg_bytes_call(T, H) / (ms_per_step / 1e3) / 1e9
     ach = alg_bytes_stream_kernel(T, H) / (stream_ms / 1e3) / 1e9
@@ -416,12 +433,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_run(K2)
-        e_ms = (time.perf_counter() - t0) * 1e3
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": world * T * K2 / (e_ms / 1e3), "unit": "tokens/s",
+        e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev)
+        e2e = {"value": whole_job_rate(world, T, K2, e_ms), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K2,
                "overlap": "double-buffered; copy-in and copy-out on their own streams"}
 
