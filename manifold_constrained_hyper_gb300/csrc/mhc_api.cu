@@ -151,8 +151,9 @@ void plan(long long T, int H, int *n_slices, int *slice_w) {
 }
 
 // Workspace: per-item partial blocks [tiles][S] of 128 x 28 fp32, then (each 256-byte
-// aligned) the shifted form's per-slice collapse sums [S][T] fp32 and its
-// publication flags [tiles][S][4] u64.
+// aligned) the shifted form's per-slice collapse sums [S][T] fp32, its
+// publication flags [tiles][S][4] u64, and the u64 epoch cell that a call
+// being captured into a CUDA graph takes its flag value from.
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 size_t partials_bytes(long long T, int S) {
     const size_t tiles = static_cast<size_t>((T + kTileT - 1) / kTileT);
@@ -162,12 +163,16 @@ size_t ssql_bytes(long long T, int S) {
     return align256(static_cast<size_t>(S) * static_cast<size_t>(T) * sizeof(float));
 }
 
+size_t flags_bytes(long long T, int S) {
+    const size_t tiles = static_cast<size_t>((T + kTileT - 1) / kTileT);
+    return align256(tiles * static_cast<size_t>(S) * 4 * sizeof(unsigned long long));
+}
+
 size_t workspace_bytes(long long T, int H) {
     if (T <= 0 || !hidden_ok(H)) return 0;
     int S = 0, w = 0;
     plan(T, H, &S, &w);
-    const size_t tiles = static_cast<size_t>((T + kTileT - 1) / kTileT);
-    return partials_bytes(T, S) + ssql_bytes(T, S) + tiles * S * 4 * sizeof(unsigned long long);
+    return partials_bytes(T, S) + ssql_bytes(T, S) + flags_bytes(T, S) + 256;
 }
 
 // bf16 [rows.., H] viewed by TMA: dim0 = hidden (box 32, 64-byte swizzle).
@@ -314,7 +319,25 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.ssql = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + partials_bytes(T, S));
     sa.flags = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) +
                                                       partials_bytes(T, S) + ssql_bytes(T, S));
-    sa.epoch = mode == FUSED_SHIFTED ? next_epoch() : 0;
+    sa.epoch = 0;
+    sa.epoch_cell = nullptr;
+    if (mode == FUSED_SHIFTED) {
+        // Flags hold a value unique to the call. A captured call replays with
+        // its launch arguments frozen, so it takes the value from a cell that
+        // a one-thread kernel advances on every replay; other calls get it
+        // from the host.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MHC_ERR_CUDA;
+        if (cap == cudaStreamCaptureStatusActive) {
+            auto *cell = reinterpret_cast<unsigned long long *>(
+                static_cast<uint8_t *>(workspace) + partials_bytes(T, S) + ssql_bytes(T, S) +
+                flags_bytes(T, S));
+            if (mhc_status s = cuda_status(launch_epoch_bump(cell, st))) return s;
+            sa.epoch_cell = cell;
+        } else {
+            sa.epoch = next_epoch();
+        }
+    }
     sa.coef = coef_args(scale, base, params);
     sa.norm_w = norm_w;
     sa.nw_bf16 = norm_dtype == MHC_BF16;

@@ -51,7 +51,8 @@ struct StreamArgs {
     // shifted form: the kernel also finishes the boundary
     float *ssql;                 // [n_slices][T] per-slice sums of the collapse's squares
     unsigned long long *flags;   // [tiles][n_slices][4] per-call epoch flags
-    unsigned long long epoch;    // this call's flag value
+    unsigned long long epoch;    // this call's flag value (epoch_cell == NULL)
+    const unsigned long long *epoch_cell;   // else: read the flag value here
     CoefArgs coef;
     const void *norm_w;          // [H] or NULL
     int nw_bf16;
@@ -89,6 +90,9 @@ cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *pos
                         const float *comb, uint16_t *out, long long T, int H, cudaStream_t s);
 cudaError_t launch_unarmed_wait(unsigned int *status, unsigned long long timeout_ns,
                                 cudaStream_t s);
+// Advances the u64 at `cell` by one (a single thread): the flag value of the
+// shifted call that follows on the stream, when that call is being captured.
+cudaError_t launch_epoch_bump(unsigned long long *cell, cudaStream_t s);
 cudaError_t launch_rcp_check(uint32_t first, unsigned long long count, unsigned long long *out,
                              cudaStream_t s);
 unsigned int *device_status_word();   // of the current device; NULL on failure

@@ -448,6 +448,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // ---------------------------------------------------- finishers
         regs_dec_finisher();
         const int q = warp & 3;
+        // this call's flag value: from the host, or (a call captured into a
+        // CUDA graph) from the workspace cell the epoch kernel just advanced
+        const unsigned long long epoch =
+            a.epoch_cell != nullptr ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell)
+                                    : a.epoch;
         float *red = reinterpret_cast<float *>(gbase + kRedOff);
         float *rsum = red + 2 * kFinThreads;
         float *consts = red + 3 * kFinThreads;
@@ -523,10 +528,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                         a.flags + (static_cast<long long>(it.tile) * n_slices + it.slice) * 4;
                     if (a.fuse_coef) {
                         named_barrier_sync(kFinBarrier, kFinThreads);
-                        if (q == 0 && lane == 0) flag_release(flag, a.epoch);
+                        if (q == 0 && lane == 0) flag_release(flag, epoch);
                     } else {
                         __syncwarp();
-                        if (lane == 0) flag_release(flag + q, a.epoch);
+                        if (lane == 0) flag_release(flag + q, epoch);
                     }
                 }
             }
@@ -553,13 +558,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             unsigned long long v[8];
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
-                                v[i] = f0 + 32 * i < nf ? flag_relaxed(fl + 4 * (f0 + 32 * i)) : a.epoch;
+                                v[i] = f0 + 32 * i < nf ? flag_relaxed(fl + 4 * (f0 + 32 * i)) : epoch;
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) seen = seen && v[i] == a.epoch;
+                            for (int i = 0; i < 8; ++i) seen = seen && v[i] == epoch;
                         }
                     } else {
                         for (int f = lane; f < nf; f += 32)
-                            seen = seen && flag_acquire(fl + 4 * f + q) == a.epoch;
+                            seen = seen && flag_acquire(fl + 4 * f + q) == epoch;
                     }
                     if (__all_sync(0xffffffffu, seen)) break;
                     if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }

@@ -233,6 +233,84 @@ def test_prefill_t8192_h7168_sampled_tokens():
     compare("shifted", gsel, o)
 
 
+# ------------------------------------------------------------------ stream capture
+
+
+@pytest.mark.parametrize("T,H", [(64, 7168), (2048, 7168)])
+def test_calls_capture_into_a_cuda_graph_and_replay_with_new_inputs(T, H):
+    """The entry points allocate nothing and never synchronise, so a decode
+    loop can capture them into a CUDA graph. Replaying the graph after new
+    inputs were written into the same buffers gives the eager results for
+    those inputs bit for bit (a single-wave and a multi-item plan; shifted,
+    unshifted and pre-only forms), so no per-call state is frozen into the
+    graph."""
+    dev = "cuda"
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    A = synth.make_inputs(T, H, seed=610 + T)
+    B = synth.make_inputs(T, H, seed=611 + T)
+    keys_bf, keys_f = ("residual", "x"), ("post", "comb", "pre_lag")
+    inp = {k: bf(A[k]) for k in keys_bf} | {k: f32(A[k]) for k in keys_f}
+    scale, base, nw = f32(A["scale"]), f32(A["base"]), f32(A["norm_w"])
+    w = ops.mhc_prepare_weight(f32(A["fn"]))
+    ws = torch.empty(ops.workspace_bytes(T, H), dtype=torch.uint8, device=dev)
+
+    def new_outs():
+        o = {}
+        for form in ("s", "u", "p"):
+            o[form] = dict(layer_input=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                           pre_out=torch.empty(T, 4, device=dev),
+                           post_out=torch.empty(T, 4, device=dev),
+                           comb_out=torch.empty(T, 4, 4, device=dev))
+            if form != "p":
+                o[form]["residual_out"] = torch.empty_like(inp["residual"])
+        return o
+
+    def run(o, stream=None):
+        for form, pl in (("s", inp["pre_lag"]), ("u", None)):
+            ops.mhc_boundary_fused(inp["x"], inp["residual"], inp["post"], inp["comb"], w, scale,
+                                   base, nw, pl, workspace=ws, stream=stream, **o[form])
+        ops.mhc_pre(inp["residual"], w, scale, base, nw, workspace=ws, stream=stream, **o["p"])
+
+    def load(d):
+        for k in keys_bf:
+            inp[k].copy_(bf(d[k]))
+        for k in keys_f:
+            inp[k].copy_(f32(d[k]))
+
+    load(B)
+    eager = new_outs()
+    run(eager)
+    torch.cuda.synchronize()
+    load(A)
+    cap = new_outs()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run(cap, stream=s)                       # warm-up on the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            run(cap, stream=s)
+    torch.cuda.synchronize()
+    g.replay()                                   # inputs A
+    torch.cuda.synchronize()
+    load(B)
+    for o in cap.values():
+        for v in o.values():
+            v.zero_()
+    torch.cuda.synchronize()
+    g.replay()                                   # inputs B, same buffers
+    torch.cuda.synchronize()
+    assert ops.mhc_get_device_status() == 0
+    for form in cap:
+        for k, v in eager[form].items():
+            got = cap[form][k]
+            if v.dtype == torch.bfloat16:
+                v, got = v.view(torch.int16), got.view(torch.int16)
+            assert torch.equal(v, got), (form, k)
+
+
 # ------------------------------------------------------------------ reciprocal
 
 
