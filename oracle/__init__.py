@@ -16,6 +16,7 @@ from .oracle import (  # noqa: F401
     coefficients,
     f32_to_bf16,
     post,
+    pre_split_k,
     sigmoid,
     sinkhorn,
     tf32_round,

@@ -222,6 +222,40 @@ static void coefficients(const float *mix, float rstd, const float *scale,
     memcpy(comb, c, sizeof c);
 }
 
+/* ---- collapse and layer RMSNorm ------------------------------------------ */
+
+/* One token: li[h] = bf16(fma chain over j from 0 of pc[j] * cur[j][h]), not
+ * flushed ([B] lagged_collapse; [P] "computing layer_input"), then the RMSNorm
+ * over H ([B] layer_input_words): out = bf16((li * rstd_li) * norm_w), or li
+ * itself without norm_w. Returns rstd_li. li is scratch of H values. */
+static float collapse_norm(const uint16_t *cur, const float *pc, const void *norm_w,
+                           int nw_bf16, const oracle_params *p, int H, uint16_t *li,
+                           uint16_t *out)
+{
+    for (int h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int j = 0; j < NHC; ++j)
+            acc = fmaf(pc[j], bf16_to_f32(cur[(int64_t)j * H + h]), acc);
+        li[h] = f32_to_bf16(acc);
+    }
+    double ssq_li = 0.0;
+    for (int h = 0; h < H; ++h) {
+        double v = bf16_to_f32(li[h]);
+        ssq_li += v * v;
+    }
+    float rstd_li = (float)(1.0 / sqrt(ssq_li / (double)H + (double)p->norm_eps));
+    if (out) {
+        for (int h = 0; h < H; ++h) {
+            if (!norm_w) { out[h] = li[h]; continue; }
+            float w = nw_bf16 ? bf16_to_f32(((const uint16_t *)norm_w)[h])
+                              : ((const float *)norm_w)[h];
+            float a = bf16_to_f32(li[h]) * rstd_li;
+            out[h] = f32_to_bf16(a * w);
+        }
+    }
+    return rstd_li;
+}
+
 /* ---- the boundary ------------------------------------------------------- */
 
 enum { ORACLE_PRE_ONLY = 0, ORACLE_FUSED_UNSHIFTED = 1, ORACLE_FUSED_SHIFTED = 2 };
@@ -300,37 +334,54 @@ void oracle_boundary(int mode, const uint16_t *x, const uint16_t *residual,
         if (post_out) memcpy(post_out + t * NHC, post, sizeof post);
         if (comb_out) memcpy(comb_out + t * NHC * NHC, comb, sizeof comb);
 
-        /* 7. collapse ([B] lagged_collapse; [P] "computing layer_input"):
-         *    li[h] = bf16(fma chain over j from 0), not flushed */
+        /* 7-8. collapse and layer RMSNorm */
         const float *pc = (mode == ORACLE_FUSED_SHIFTED) ? pre_lag + t * NHC : pre;
-        for (int h = 0; h < H; ++h) {
-            float acc = 0.0f;
-            for (int j = 0; j < NHC; ++j)
-                acc = fmaf(pc[j], bf16_to_f32(cur[(int64_t)j * H + h]), acc);
-            li[h] = f32_to_bf16(acc);
-        }
-
-        /* 8. RMSNorm of the collapse over H ([B] layer_input_words):
-         *    out = bf16((li * rstd_li) * norm_w) */
-        double ssq_li = 0.0;
-        for (int h = 0; h < H; ++h) {
-            double v = bf16_to_f32(li[h]);
-            ssq_li += v * v;
-        }
-        float rstd_li = (float)(1.0 / sqrt(ssq_li / (double)H + (double)p->norm_eps));
+        float rstd_li = collapse_norm(cur, pc, norm_w, nw_bf16, p, H, li,
+                                      layer_input ? layer_input + t * H : NULL);
         if (rstd_li_out) rstd_li_out[t] = rstd_li;
-        if (layer_input) {
-            for (int h = 0; h < H; ++h) {
-                if (!norm_w) { layer_input[t * H + h] = li[h]; continue; }
-                float w = nw_bf16 ? bf16_to_f32(((const uint16_t *)norm_w)[h])
-                                  : ((const float *)norm_w)[h];
-                float a = bf16_to_f32(li[h]) * rstd_li;
-                layer_input[t * H + h] = f32_to_bf16(a * w);
-            }
-        }
     }
     free(r);
     free(cur);
+    free(li);
+}
+
+/*
+ * Pre from split-K mixes ([P] "square sum and RMSNorm", path 1 with split-K,
+ * and "explaining split-K"): the previous GEMM split the 4H-long contraction
+ * into S parts and left its partial mixes dot_mix [S][T][24] and partial sums
+ * of squares of the flattened residual sqrsum [S][T]. Here
+ *   mix[t][n] = sum over s of dot_mix[s][t][n]   (summed in double, rounded once)
+ *   ssq[t]    = sum over s of sqrsum[s][t]       (in double)
+ * and rstd, pre / post / comb, the collapse of the residual with this pre and
+ * the layer RMSNorm follow exactly as in oracle_boundary mode 0.
+ */
+void oracle_pre_split_k(const uint16_t *residual, const float *dot_mix, const float *sqrsum,
+                        int S, const float *scale, const float *base, const void *norm_w,
+                        int nw_bf16, const oracle_params *p, int64_t T, int H,
+                        uint16_t *layer_input, float *pre_out, float *post_out,
+                        float *comb_out)
+{
+    const int64_t K = (int64_t)NHC * H;
+    uint16_t *li = (uint16_t *)malloc(sizeof(uint16_t) * H);
+    if (!li) return;
+    for (int64_t t = 0; t < T; ++t) {
+        float mix[MIXES];
+        for (int n = 0; n < MIXES; ++n) {
+            double acc = 0.0;
+            for (int s = 0; s < S; ++s) acc += (double)dot_mix[((int64_t)s * T + t) * MIXES + n];
+            mix[n] = (float)acc;
+        }
+        double ssq = 0.0;
+        for (int s = 0; s < S; ++s) ssq += (double)sqrsum[(int64_t)s * T + t];
+        float rstd = (float)(1.0 / sqrt(ssq / (double)K + (double)p->hc_norm_eps));
+        float pre[NHC], post[NHC], comb[NHC * NHC];
+        coefficients(mix, rstd, scale, base, p, pre, post, comb);
+        if (pre_out) memcpy(pre_out + t * NHC, pre, sizeof pre);
+        if (post_out) memcpy(post_out + t * NHC, post, sizeof post);
+        if (comb_out) memcpy(comb_out + t * NHC * NHC, comb, sizeof comb);
+        collapse_norm(residual + t * K, pre, norm_w, nw_bf16, p, H, li,
+                      layer_input ? layer_input + t * H : NULL);
+    }
     free(li);
 }
 

@@ -77,6 +77,9 @@ def _load():
         lib.oracle_tf32_round.argtypes = [P, i64, P]
         lib.oracle_sigmoid.argtypes = [P, i64, P]
         lib.oracle_sinkhorn.argtypes = [P, i64, ctypes.c_int, ctypes.c_float]
+        lib.oracle_pre_split_k.argtypes = ([P, P, P, ctypes.c_int, P, P, P, ctypes.c_int,
+                                            ctypes.POINTER(_Params), i64, ctypes.c_int]
+                                           + [P] * 4)
         _lib = lib
     return _lib
 
@@ -161,6 +164,36 @@ def coefficients(mix, rstd, scale, base, params: OracleParams | None = None):
                                 _ptr(_c(base, np.float32)), ctypes.byref(p), T,
                                 _ptr(pre), _ptr(post_), _ptr(comb))
     return pre, post_, comb
+
+
+def pre_split_k(residual, dot_mix, sqrsum, scale, base, norm_w=None,
+                params: OracleParams | None = None):
+    """Pre from split-K partial mixes dot_mix [S, T, 24] and partial sums of
+    squares sqrsum [S, T]. Returns a dict: layer_input (uint16 [T, H]), pre,
+    post, comb."""
+    params = params or OracleParams()
+    residual = _c(residual, np.uint16)
+    T, n, H = residual.shape
+    assert n == 4
+    dot_mix = _c(dot_mix, np.float32)
+    sqrsum = _c(sqrsum, np.float32)
+    S = dot_mix.shape[0]
+    assert dot_mix.shape == (S, T, 24) and sqrsum.shape == (S, T)
+    nw_bf16 = 0
+    if norm_w is not None:
+        if norm_w.dtype == np.uint16:
+            nw_bf16 = 1
+        else:
+            norm_w = _c(norm_w, np.float32)
+    out = {"layer_input": np.empty((T, H), np.uint16), "pre": np.empty((T, 4), np.float32),
+           "post": np.empty((T, 4), np.float32), "comb": np.empty((T, 4, 4), np.float32)}
+    p = params._c()
+    _load().oracle_pre_split_k(_ptr(residual), _ptr(dot_mix), _ptr(sqrsum), S,
+                               _ptr(_c(scale, np.float32)), _ptr(_c(base, np.float32)),
+                               _ptr(norm_w), nw_bf16, ctypes.byref(p), T, H,
+                               _ptr(out["layer_input"]), _ptr(out["pre"]), _ptr(out["post"]),
+                               _ptr(out["comb"]))
+    return out
 
 
 def boundary(mode: int, residual, fn, scale, base, norm_w=None, *, x=None,

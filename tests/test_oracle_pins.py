@@ -414,3 +414,57 @@ def test_oracle_is_deterministic_and_token_independent():
     b = _shifted(sub, sub["pre_lag"], norm_w=d["norm_w"])
     for k in ("residual_out", "layer_input", "pre", "post", "comb", "mix"):
         assert np.array_equal(a[k][2:4], b[k]), k
+
+
+# ---------------------------------------------------------------- split-K pre
+
+
+@pytest.mark.parametrize("weights", [[1.0], [0.5, 0.25, 0.25], [0.5, 0.25, 0.125, 0.125]])
+def test_split_k_pre_of_exact_splits_equals_the_boundary(weights):
+    """[P] "explaining split-K": the pure path sums the previous GEMM's
+    partial mixes and partial sums of squares over the K splits. On a
+    small-integer residual the 4H sum of squares is an exact integer, and
+    splitting the boundary's own mixes and sum of squares by powers of two
+    is exact, so the split-K pre must reproduce pre-only boundary bit for
+    bit: same rstd, coefficients, collapse and layer RMSNorm."""
+    T, H = 5, 64
+    rng = np.random.default_rng(57)
+    d = synth.make_inputs(T, H, seed=57)
+    d["residual"] = _bf16(rng.integers(-2, 3, size=(T, 4, H)).astype(np.float32))
+    ref = orc.boundary(orc.MODE_PRE_ONLY, d["residual"], d["fn"], d["scale"], d["base"],
+                       d["norm_w"])
+    cur = B2F(d["residual"]).astype(np.float64).reshape(T, -1)
+    ssq = (cur * cur).sum(axis=1)                          # exact small integers
+    w = np.array(weights, np.float32)
+    dot_mix = (w[:, None, None] * ref["mix"][None]).astype(np.float32)
+    sqrsum = (w[:, None] * ssq.astype(np.float32)[None]).astype(np.float32)
+    assert np.array_equal(dot_mix.astype(np.float64).sum(0), ref["mix"].astype(np.float64))
+    out = orc.pre_split_k(d["residual"], dot_mix, sqrsum, d["scale"], d["base"], d["norm_w"])
+    for k in ("pre", "post", "comb", "layer_input"):
+        assert np.array_equal(out[k], ref[k]), k
+
+
+def test_split_k_single_split_rstd_and_coefficients():
+    """With one split the mixes pass through unchanged and rstd is
+    1 / sqrt(sqrsum / 4H + eps), computed here in numpy double; the
+    coefficients must then equal the coefficient routine's on those
+    values."""
+    T, H = 4, 32
+    rng = np.random.default_rng(58)
+    d = synth.make_inputs(T, H, seed=58)
+    dot_mix = rng.normal(0, 3, size=(1, T, 24)).astype(np.float32)
+    sqrsum = rng.uniform(10, 500, size=(1, T)).astype(np.float32)
+    out = orc.pre_split_k(d["residual"], dot_mix, sqrsum, d["scale"], d["base"], None)
+    rstd = (1.0 / np.sqrt(sqrsum[0].astype(np.float64) / (4 * H) + 1e-6)).astype(np.float32)
+    pre, post, comb = orc.coefficients(dot_mix[0], rstd, d["scale"], d["base"])
+    assert np.array_equal(out["pre"], pre)
+    assert np.array_equal(out["post"], post)
+    assert np.array_equal(out["comb"], comb)
+    # without norm_w the layer input is the raw collapse with this pre
+    cur = B2F(d["residual"]).astype(np.float32)
+    acc = np.zeros((T, H), np.float32)
+    for j in range(4):
+        acc = (pre[:, j:j + 1] * cur[:, j] + acc).astype(np.float32)
+    want = _bf16(acc)
+    diff = np.abs(out["layer_input"].astype(np.int32) - want.astype(np.int32))
+    assert diff.max() <= 1          # numpy's separately rounded multiply-add vs the fma chain
