@@ -176,6 +176,27 @@ mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
 /* counterpart of this entry point.                                         */
 
 /*
+ * Unshifted pre from split-K mixes ("The Hyper Connection Preprocessing GPU
+ * Kernel Study", the pure path: "square sum and RMSNorm" path 1 and
+ * "explaining split-K"): a previous GEMM split the 4H-long contraction of the
+ * flattened residual with fn into n_splits parts and left
+ *   dot_mix [n_splits, T, 24] fp32   partial mixes (no TF32 rounding implied),
+ *   sqrsum  [n_splits, T]     fp32   partial sums of squares of the residual.
+ * mix = sum of the splits, ssq = sum of the splits (each in split order, in
+ * fp32); rstd = rsqrt(ssq / 4H + hc_norm_eps); pre / post / comb as in
+ * mhc_pre; layer_input = the collapse of residual [T, 4, H] with this pre,
+ * RMS-normed with norm_w (or the raw collapse when norm_w is NULL).
+ * n_splits in [1, 64] (the page's kernel takes 1, 2, 4, 8 or 16), else
+ * MHC_ERR_SHAPE. No workspace. Outputs as in mhc_pre; none may alias an
+ * input. Two kernels on `stream` (coefficients, then the collapse).
+ */
+mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const float *sqrsum,
+                           int n_splits, const float *scale, const float *base,
+                           const void *norm_w, mhc_dtype norm_dtype, const mhc_params *params,
+                           int64_t tokens, int hidden, uint16_t *layer_input, float *pre_out,
+                           float *post_out, float *comb_out, void *stream);
+
+/*
  * mhc_boundary_fused without a workspace, for callers that cannot allocate
  * device memory: code running where cudaMalloc is not permitted or not
  * wanted, such as a serving engine whose memory planner owns every device

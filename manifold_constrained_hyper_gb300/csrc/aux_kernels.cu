@@ -140,6 +140,44 @@ __global__ void __launch_bounds__(kCoefThreads, 2) coefficients_kernel(const Fin
                             a.post_out, a.comb_out);
 }
 
+// ------------------------------------------------------------ coefficients (split-K)
+// The pure pre path's inputs ("The Hyper Connection Preprocessing GPU Kernel
+// Study", square sum and RMSNorm with split-K): partial mixes dot_mix
+// [S][T][24] and partial sums of squares sqrsum [S][T]. 32 tokens per block;
+// thread p < 768 owns flat value p of the block's 32 x 24 mixes (consecutive
+// threads read consecutive floats), threads 768..799 the 32 sums of squares;
+// each sums its value over the splits in split order. Then warp 0 forms the
+// coefficients, one thread per token.
+__global__ void __launch_bounds__(kCoefThreads, 2)
+coefficients_split_k_kernel(const float *__restrict__ dot_mix, const float *__restrict__ sqrsum,
+                            int n_splits, const FinishArgs a) {
+    __shared__ float red[kPartVals][kCoefTokens];
+    __shared__ float consts[32];
+    const int p = threadIdx.x, warp = p >> 5, lane = p & 31;
+    const long long t0 = static_cast<long long>(blockIdx.x) * kCoefTokens;
+    stage_coef_consts(a.coef, consts, p);
+    const int j = p < 24 * kCoefTokens ? p / 24 : p - 24 * kCoefTokens;
+    const int m = p < 24 * kCoefTokens ? p - 24 * j : 24;
+    if (t0 + j < a.T) {
+        const float *src = m < 24 ? dot_mix + t0 * 24 + p : sqrsum + t0 + j;
+        const long long step = m < 24 ? a.T * 24 : a.T;
+        float v = 0.f;
+        for (int s = 0; s < n_splits; s += 16) {
+            float w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = s + i < n_splits ? __ldg(src + (s + i) * step) : 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (s + i < n_splits) v += w[i];
+        }
+        red[m][j] = v;
+    }
+    __syncthreads();
+    if (warp == 0 && t0 + lane < a.T)
+        coefficients_thread(&red[0][lane], kCoefTokens, consts, a.coef, a.H, t0 + lane, a.pre_out,
+                            a.post_out, a.comb_out);
+}
+
 // ------------------------------------------------------------ collapse (unshifted)
 // One 128-thread block per token, after the coefficients: collapse the
 // token's 4 updated streams with this boundary's pre into shared memory,
@@ -278,6 +316,13 @@ cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, coefficients_kernel, a);
+}
+
+cudaError_t launch_coefficients_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
+                                        const FinishArgs &a, cudaStream_t s) {
+    const unsigned blocks = static_cast<unsigned>((a.T + kCoefTokens - 1) / kCoefTokens);
+    coefficients_split_k_kernel<<<blocks, kCoefThreads, 0, s>>>(dot_mix, sqrsum, n_splits, a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s) {

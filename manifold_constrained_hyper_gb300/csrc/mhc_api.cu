@@ -447,6 +447,56 @@ mhc_status mhc_pre(const uint16_t *residual, const void *weight, const float *sc
                         pre_out, post_out, comb_out, workspace, workspace_bytes, stream);
 }
 
+mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const float *sqrsum,
+                           int n_splits, const float *scale, const float *base,
+                           const void *norm_w, mhc_dtype norm_dtype, const mhc_params *params,
+                           int64_t tokens, int hidden, uint16_t *layer_input, float *pre_out,
+                           float *post_out, float *comb_out, void *stream) {
+    const long long T = tokens;
+    const int H = hidden;
+    if (T < 0 || n_splits < 1 || n_splits > kMaxSplits) return MHC_ERR_SHAPE;
+    if (mhc_status s = check_params(params)) return s;
+    if (!hidden_ok(H)) return MHC_ERR_UNSUPPORTED;
+    if (norm_w && norm_dtype != MHC_F32 && norm_dtype != MHC_BF16) return MHC_ERR_SHAPE;
+    if (T == 0) return MHC_OK;
+    const void *need[] = {residual, dot_mix, sqrsum, scale, base, layer_input, pre_out, post_out,
+                          comb_out};
+    for (const void *p : need)
+        if (!p) return MHC_ERR_NULL;
+    const void *al[] = {residual, dot_mix, sqrsum, scale, base, norm_w, layer_input, pre_out,
+                        post_out, comb_out};
+    for (const void *p : al)
+        if (p && !aligned16(p)) return MHC_ERR_ALIGN;
+    const size_t nres = static_cast<size_t>(T) * 4 * H * 2, nx = static_cast<size_t>(T) * H * 2;
+    const size_t n4 = static_cast<size_t>(T) * 16, n16 = static_cast<size_t>(T) * 64;
+    const size_t nmix = static_cast<size_t>(n_splits) * T * 24 * 4;
+    const size_t nsq = static_cast<size_t>(n_splits) * T * 4;
+    const size_t nw = norm_w ? static_cast<size_t>(H) * (norm_dtype == MHC_BF16 ? 2 : 4) : 0;
+    const Range ins[] = {{residual, nres}, {dot_mix, nmix}, {sqrsum, nsq}, {scale, 12},
+                         {base, 96}, {norm_w, nw}};
+    const Range outs[] = {{layer_input, nx}, {pre_out, n4}, {post_out, n4}, {comb_out, n16}};
+    if (aliasing(outs, 4, ins, 6, nullptr, nullptr)) return MHC_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    FinishArgs fa;
+    fa.partials = nullptr;
+    fa.n_slices = 0;
+    fa.coef = coef_args(scale, base, params);
+    fa.norm_w = norm_w;
+    fa.nw_bf16 = norm_dtype == MHC_BF16;
+    fa.cur = residual;
+    fa.layer_input = layer_input;
+    fa.pre_out = pre_out;
+    fa.post_out = post_out;
+    fa.comb_out = comb_out;
+    fa.T = T;
+    fa.H = H;
+    if (mhc_status s = cuda_status(launch_coefficients_split_k(dot_mix, sqrsum, n_splits, fa, st)))
+        return s;
+    return cuda_status(launch_collapse_unshifted(fa, st));
+}
+
 mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual, const float *post,
                               const float *comb, const float *pre_lag, const void *weight,
                               const float *scale, const float *base, const void *norm_w,

@@ -76,6 +76,7 @@ struct FinishArgs {
 };
 
 constexpr int kGridCap = 152;                       // persistent CTAs: one per GB300 SM
+constexpr int kMaxSplits = 64;                      // split-K pre: most K splits accepted
 
 size_t stream_smem_bytes();
 // Persistent streaming kernel over n_items = tiles x n_slices work items
@@ -85,6 +86,8 @@ cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x
                           int grid, cudaStream_t s);
 cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
+cudaError_t launch_coefficients_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
+                                        const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s);
 cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *post,
                         const float *comb, uint16_t *out, long long T, int H, cudaStream_t s);

@@ -27,7 +27,7 @@ EXPORTS = ("mhc_weight_bytes", "mhc_prepare_weight", "mhc_post", "mhc_workspace_
            "mhc_pre", "mhc_boundary_fused", "mhc_get_device_status", "mhc_last_timeout_site",
            "mhc_status_string", "mhc_set_wait_timeout_ns", "mhc_debug_unarmed_wait",
            "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc",
-           "mhc_debug_rcp_check")
+           "mhc_debug_rcp_check", "mhc_pre_split_k")
 
 
 class MhcError(RuntimeError):
@@ -88,6 +88,7 @@ def load():
         "mhc_debug_unarmed_wait": (i32, [P]),
         "mhc_debug_record_between": (None, [P]),
         "mhc_debug_rcp_check": (i32, [ctypes.c_uint32, ctypes.c_uint64, P, P]),
+        "mhc_pre_split_k": (i32, [P, P, P, i32, P, P, P, i32, PP, i64, i32, P, P, P, P, P]),
         "mhc_plan": (i32, [i64, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     }
     for name, (res, args) in sig.items():
@@ -196,6 +197,31 @@ def mhc_pre(residual, weight, scale, base, norm_w=None, params: Params | None = 
     _check(load().mhc_pre(_p(residual), _p(weight), _p(scale), _p(base), _p(nw), nwt,
                           ctypes.byref(p), T, H, _p(li), _p(pr), _p(po), _p(cb), _p(ws),
                           ws.numel() * ws.element_size(), _stream(stream)), "mhc_pre")
+    return li, pr, po, cb
+
+
+def mhc_pre_split_k(residual, dot_mix, sqrsum, scale, base, norm_w=None,
+                    params: Params | None = None, *, layer_input=None, pre_out=None,
+                    post_out=None, comb_out=None, stream=None):
+    """Unshifted pre from split-K partial mixes dot_mix [S, T, 24] and partial
+    sums of squares sqrsum [S, T]: returns (layer_input, pre, post, comb)."""
+    _bf16(residual, "residual"), _f32(dot_mix, "dot_mix"), _f32(sqrsum, "sqrsum")
+    T, n, H = residual.shape
+    S = dot_mix.shape[0]
+    if tuple(dot_mix.shape) != (S, T, 24) or tuple(sqrsum.shape) != (S, T):
+        raise ValueError("dot_mix must be [S, T, 24] and sqrsum [S, T]")
+    params = params or Params()
+    dev = residual.device
+    li = layer_input if layer_input is not None else torch.empty(T, H, dtype=torch.bfloat16,
+                                                                 device=dev)
+    pr = pre_out if pre_out is not None else torch.empty(T, 4, device=dev)
+    po = post_out if post_out is not None else torch.empty(T, 4, device=dev)
+    cb = comb_out if comb_out is not None else torch.empty(T, 4, 4, device=dev)
+    nw, nwt = _nw(norm_w)
+    p = params.c()
+    _check(load().mhc_pre_split_k(_p(residual), _p(dot_mix), _p(sqrsum), S, _p(scale), _p(base),
+                                  _p(nw), nwt, ctypes.byref(p), T, H, _p(li), _p(pr), _p(po),
+                                  _p(cb), _stream(stream)), "mhc_pre_split_k")
     return li, pr, po, cb
 
 

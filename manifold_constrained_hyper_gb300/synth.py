@@ -22,6 +22,7 @@ path and the CPU oracle consume the very same bytes.
 from __future__ import annotations
 
 import itertools
+import math
 
 import numpy as np
 import torch
@@ -111,6 +112,20 @@ def workload_inputs(name: str, **overrides) -> dict:
     cfg = dict(WORKLOADS[name])
     cfg.update(overrides)
     return make_inputs(**cfg)
+
+
+def make_split_k_inputs(T: int, H: int, S: int, seed: int, **kw) -> dict:
+    """Inputs of one split-K pre call: make_inputs' tensors plus the previous
+    GEMM's outputs stood in for by seeded random numbers: dot_mix [S, T, 24]
+    ~ N(0, 1 / sqrt(S)) (the mixes of N(0, 1) residuals with fn ~ N(0,
+    1 / sqrt(4H)) are about N(0, 1)), and sqrsum [S, T] ~ (4H / S) * U(0.8,
+    1.2) (positive, summing to about 4H)."""
+    d = make_inputs(T, H, seed, **kw)
+    g = torch.Generator("cpu").manual_seed(int(seed) + 7)
+    d["dot_mix"] = (torch.randn(S, T, 24, generator=g) / math.sqrt(S)).numpy().astype(np.float32)
+    d["sqrsum"] = ((4.0 * H / S) * (0.8 + 0.4 * torch.rand(S, T, generator=g))).numpy().astype(
+        np.float32)
+    return d
 
 
 def bf16_bits_to_float(a: np.ndarray) -> np.ndarray:

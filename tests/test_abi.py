@@ -98,3 +98,14 @@ def test_argument_errors_before_any_device_work(lib):
     assert lib.mhc_debug_rcp_check(0, 16, _P(A + 4), None) == 2
     assert lib.mhc_debug_rcp_check(0xFFFFFFF0, 17, _P(A), None) == 3
     assert lib.mhc_debug_rcp_check(0, 0, _P(A), None) == 0
+    # split-K pre: splits out of range, NULL sums, misaligned mixes, T == 0
+    sk = [_P(A), _P(A * 2), _P(A * 3)]
+    rest = [_P(A * 4), _P(A * 5), None, 0, ctypes.byref(p), 4, 256, _P(A * 8), _P(A * 9),
+            _P(A * 10), _P(A * 11), None]
+    assert lib.mhc_pre_split_k(*sk, 0, *rest) == 3
+    assert lib.mhc_pre_split_k(*sk, 65, *rest) == 3
+    assert lib.mhc_pre_split_k(_P(A), _P(A * 2), None, 4, *rest) == 1
+    assert lib.mhc_pre_split_k(_P(A), _P(A * 2 + 4), _P(A * 3), 4, *rest) == 2
+    rest0 = list(rest)
+    rest0[5] = 0
+    assert lib.mhc_pre_split_k(*sk, 4, *rest0) == 0
