@@ -178,6 +178,101 @@ coefficients_split_k_kernel(const float *__restrict__ dot_mix, const float *__re
                             a.post_out, a.comb_out);
 }
 
+// ------------------------------------------------------------ split-K pre, one kernel
+// One 128-thread block per token. Warp 0 sums the token's splits (lanes 0-23
+// the mixes, lane 24 the sum of squares), forms rstd and pre (lanes 0-3) and
+// hands pre to warps 1-3, which collapse the token's 4 streams with it and
+// write the RMS-normed layer input ("computing pre_mix early" on the page:
+// the collapse needs pre only); meanwhile lane 0 of warp 0 forms post and
+// the Sinkhorn comb. Same arithmetic and order as the two-kernel form.
+constexpr int kSkThreads = 128;
+constexpr int kSkCollapse = kSkThreads - 32;
+
+__global__ void __launch_bounds__(kSkThreads)
+pre_split_k_kernel(const float *__restrict__ dot_mix, const float *__restrict__ sqrsum,
+                   int n_splits, const FinishArgs a) {
+    extern __shared__ uint4 li_s[];            // [H/8]
+    __shared__ float vals[kPartVals];
+    __shared__ float consts[32];
+    __shared__ float pre_s[4];
+    __shared__ float red_s[kSkCollapse / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long t = blockIdx.x;
+    if (warp == 0) {
+        stage_coef_consts(a.coef, consts, lane);
+        float v = 0.f;
+        if (lane < kPartVals) {
+            const float *src = lane < 24 ? dot_mix + t * 24 + lane : sqrsum + t;
+            const long long step = lane < 24 ? a.T * 24 : a.T;
+            for (int s = 0; s < n_splits; s += 16) {
+                float w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = s + i < n_splits ? __ldg(src + (s + i) * step) : 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (s + i < n_splits) v += w[i];
+            }
+            vals[lane] = v;
+        }
+        __syncwarp();
+        if (lane < 4) {
+            const float rstd =
+                rsqrtf(__fdiv_rn(vals[24], static_cast<float>(4 * a.H)) + a.coef.hc_norm_eps);
+            pre_s[lane] = sigmoid_clamped(fmaf(v * rstd, consts[0], consts[3 + lane])) +
+                          a.coef.hc_pre_eps;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            coefficients_thread(vals, 1, consts, a.coef, a.H, t, a.pre_out, a.post_out,
+                                a.comb_out);
+        return;
+    }
+    const int ct = tid - 32;
+    const uint64_t p2[4] = {f2_pack(pre_s[0], pre_s[0]), f2_pack(pre_s[1], pre_s[1]),
+                            f2_pack(pre_s[2], pre_s[2]), f2_pack(pre_s[3], pre_s[3])};
+    const int units = a.H / 8;
+    uint64_t sq2 = 0;
+    for (int u = ct; u < units; u += kSkCollapse) {
+        uint32_t cs[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 r = ld_global_nc_v4(a.cur + (t * 4 + j) * a.H + 8LL * u);
+            cs[j][0] = r.x; cs[j][1] = r.y; cs[j][2] = r.z; cs[j][3] = r.w;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            uint64_t acc = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc = fma2(p2[j], bf2_unpack(cs[j][p]), acc);
+            w[p] = bf2_pack_rn(acc);
+            const uint64_t lv = bf2_unpack(w[p]);
+            sq2 = fma2(lv, lv, sq2);
+        }
+        li_s[u] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    uint16_t *row = a.layer_input + t * a.H;
+    if (a.norm_w == nullptr) {
+        for (int u = ct; u < units; u += kSkCollapse)
+            *reinterpret_cast<uint4 *>(row + 8LL * u) = li_s[u];
+        return;
+    }
+    float sq = f2_lo(sq2) + f2_hi(sq2);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+    if (lane == 0) red_s[warp - 1] = sq;
+    named_barrier_sync(1, kSkCollapse);
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSkCollapse / 32; ++w) tot += red_s[w];
+    const float rstd_li = rsqrtf(__fdiv_rn(tot, static_cast<float>(a.H)) + a.coef.norm_eps);
+    for (int u = ct; u < units; u += kSkCollapse)
+        *reinterpret_cast<uint4 *>(row + 8LL * u) =
+            norm8(li_s[u], rstd_li, a.norm_w, a.nw_bf16, 8LL * u);
+}
+
 // ------------------------------------------------------------ collapse (unshifted)
 // One 128-thread block per token, after the coefficients: collapse the
 // token's 4 updated streams with this boundary's pre into shared memory,
@@ -322,6 +417,20 @@ cudaError_t launch_coefficients_split_k(const float *dot_mix, const float *sqrsu
                                         const FinishArgs &a, cudaStream_t s) {
     const unsigned blocks = static_cast<unsigned>((a.T + kCoefTokens - 1) / kCoefTokens);
     coefficients_split_k_kernel<<<blocks, kCoefThreads, 0, s>>>(dot_mix, sqrsum, n_splits, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
+                               const FinishArgs &a, cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(a.H) * 2;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(pre_split_k_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    pre_split_k_kernel<<<static_cast<unsigned>(a.T), kSkThreads, smem, s>>>(dot_mix, sqrsum,
+                                                                          n_splits, a);
     return cudaGetLastError();
 }
 

@@ -126,6 +126,7 @@ bool aliasing(const Range *outs, int no, const Range *ins, int ni, const void *m
 // smallest larger one. A pure function of (T, H), so the workspace size is
 // too.
 constexpr double kItemCost = 2.0;
+constexpr long long kSplitKOneKernelTokens = 1024;
 void plan(long long T, int H, int *n_slices, int *slice_w) {
     const int chunks = H / kChunk;
     const long long tiles = (T + kTileT - 1) / kTileT;
@@ -492,6 +493,11 @@ mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const
     fa.comb_out = comb_out;
     fa.T = T;
     fa.H = H;
+    // few tokens: one kernel, the collapse overlapping the coefficients
+    // (latency); many: coefficients for 32 tokens per block, then the
+    // collapse (bandwidth)
+    if (T <= kSplitKOneKernelTokens)
+        return cuda_status(launch_pre_split_k(dot_mix, sqrsum, n_splits, fa, st));
     if (mhc_status s = cuda_status(launch_coefficients_split_k(dot_mix, sqrsum, n_splits, fa, st)))
         return s;
     return cuda_status(launch_collapse_unshifted(fa, st));

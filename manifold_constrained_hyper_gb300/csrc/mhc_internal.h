@@ -86,6 +86,8 @@ cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x
                           int grid, cudaStream_t s);
 cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
+cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
+                               const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_coefficients_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
                                         const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s);
