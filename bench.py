@@ -332,6 +332,56 @@ def measure_decode(dev, token_counts=None):
     return out
 
 
+def measure_split_k(dev):
+    """Per-call time of the split-K pre at the shapes the FlashInfer page
+    times its pure path on (tokens x hidden: 4096 x 4096, 4096 x 7168,
+    128 x 7168; one split), from a CUDA graph of 20 calls. Inputs are seeded
+    on the device; the 4096-token cases exceed L2."""
+    import torch
+    from manifold_constrained_hyper_gb300 import ops, synth
+    out = {"unit": "us/call", "splits": 1, "cases": {}}
+    for T, H in ((4096, 4096), (4096, 7168), (128, 7168)):
+        d = synth.make_inputs_device(T, H, 3, dev)
+        f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+        g = torch.Generator(dev).manual_seed(5)
+        dm = torch.randn(1, T, 24, device=dev, generator=g)
+        sq = 4.0 * H * (0.8 + 0.4 * torch.rand(1, T, device=dev, generator=g))
+        scale, base, nw = f32(d["scale"]), f32(d["base"]), f32(d["norm_w"])
+        o = dict(layer_input=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                 pre_out=torch.empty(T, 4, device=dev), post_out=torch.empty(T, 4, device=dev),
+                 comb_out=torch.empty(T, 4, 4, device=dev))
+        res = d["residual_dev"]
+
+        def call(s=None):
+            ops.mhc_pre_split_k(res, dm, sq, scale, base, nw, stream=s, **o)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        st = torch.cuda.Stream(device=dev)
+        st.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(st):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=st):
+                for _ in range(20):
+                    call(st)
+        torch.cuda.synchronize()
+        gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / 20
+        byts = T * (8 * H + 2 * H + 196) + 4 * H
+        peak, _ = measured_peaks()
+        out["cases"][f"{T}x{H}"] = {"us": us, "gbps": byts / us / 1e3,
+                                    "frac_of_peak": byts / us / 1e3 / peak}
+        del gr
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -493,6 +543,9 @@ def run_ours(args):
     decode = None
     if not args.no_decode:
         decode = measure_decode(dev)
+    split_k = None
+    if not args.no_decode:
+        split_k = measure_split_k(dev)
 
     S, sw = ops.plan(T, H)
     line = {
@@ -515,6 +568,7 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": 2 * K,
         "decode": decode,
+        "pre_split_k": split_k,
         "clocks": clk.summary(),
     }
     if rank == 0:
@@ -534,7 +588,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
-                    help="skip the decode-latency sweep (1-64 tokens)")
+                    help="skip the decode-latency sweep (1-64 tokens) and the split-K pre timings")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-tokens", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=0,
