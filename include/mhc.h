@@ -68,6 +68,12 @@ typedef struct {
     float sinkhorn_eps;  /* softmax floor and Sinkhorn denominator eps */
     float norm_eps;      /* eps of the layer RMSNorm of the collapse (over H) */
     int sinkhorn_iters;  /* >= 1: one column step, then iters-1 (row, column) steps */
+    int batch_invariant; /* nonzero: every output of a token is bitwise the same
+                          * whatever the batch it comes in (its size, its
+                          * position): the hidden-slice plan then depends on
+                          * the hidden size only and every reduction runs in
+                          * one fixed order. The pages have no counterpart.
+                          * Costs latency on small batches (fewer slices). */
 } mhc_params;
 
 /* Element type of norm_w. The DeepSeek boundary kernel reads bf16 weights;

@@ -127,6 +127,22 @@ bool aliasing(const Range *outs, int no, const Range *ins, int ni, const void *m
 // too.
 constexpr double kItemCost = 2.0;
 constexpr long long kSplitKOneKernelTokens = 1024;
+// The batch-invariant plan: a function of H alone, the item size the plan
+// converges to for large T (the largest of at most 8 chunks that divides H/32
+// with at most kGridCap slices, else the smallest larger one).
+void plan_invariant(int H, int *n_slices, int *slice_w) {
+    const int chunks = H / kChunk;
+    int d = 0;
+    for (int c = chunks < 8 ? chunks : 8; c >= 1 && d == 0; --c)
+        if (chunks % c == 0 && chunks / c <= kGridCap) d = c;
+    if (d == 0) {
+        d = 9;
+        while (chunks % d || chunks / d > kGridCap) ++d;
+    }
+    *n_slices = chunks / d;
+    *slice_w = d * kChunk;
+}
+
 void plan(long long T, int H, int *n_slices, int *slice_w) {
     const int chunks = H / kChunk;
     const long long tiles = (T + kTileT - 1) / kTileT;
@@ -169,11 +185,18 @@ size_t flags_bytes(long long T, int S) {
     return align256(tiles * static_cast<size_t>(S) * 4 * sizeof(unsigned long long));
 }
 
+size_t workspace_layout_bytes(long long T, int S) {
+    return partials_bytes(T, S) + ssql_bytes(T, S) + flags_bytes(T, S) + 256;
+}
+
+// Enough for the plan of either mode (default and batch-invariant).
 size_t workspace_bytes(long long T, int H) {
     if (T <= 0 || !hidden_ok(H)) return 0;
-    int S = 0, w = 0;
+    int S = 0, w = 0, Si = 0, wi = 0;
     plan(T, H, &S, &w);
-    return partials_bytes(T, S) + ssql_bytes(T, S) + flags_bytes(T, S) + 256;
+    plan_invariant(H, &Si, &wi);
+    const size_t a = workspace_layout_bytes(T, S), b = workspace_layout_bytes(T, Si);
+    return a > b ? a : b;
 }
 
 // bf16 [rows.., H] viewed by TMA: dim0 = hidden (box 32, 64-byte swizzle).
@@ -296,8 +319,12 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     if (mhc_status s = current_device(&dev)) return s;
     if (!get_encoder()) return MHC_ERR_CUDA;
 
+    const bool invariant = params->batch_invariant != 0;
     int S = 0, w = 0;
-    plan(T, H, &S, &w);
+    if (invariant)
+        plan_invariant(H, &S, &w);
+    else
+        plan(T, H, &S, &w);
     CUtensorMap m_res, m_x, m_rout;
     if (!encode_cached(0, &m_res, residual, H, T)) return MHC_ERR_CUDA;
     m_x = m_rout = m_res;
@@ -357,7 +384,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     if (mode == FUSED_SHIFTED && (S > grid || w / kChunk > 8)) return MHC_ERR_UNSUPPORTED;
     // a single wave of items: the shifted form's finishers form the
     // coefficients too (no second kernel)
-    sa.fuse_coef = mode == FUSED_SHIFTED && items <= grid;
+    sa.fuse_coef = mode == FUSED_SHIFTED && items <= grid && !invariant;
     if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, sa, S,
                                                  static_cast<int>(items), grid, st)))
         return s;
@@ -496,7 +523,7 @@ mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const
     // few tokens: one kernel, the collapse overlapping the coefficients
     // (latency); many: coefficients for 32 tokens per block, then the
     // collapse (bandwidth)
-    if (T <= kSplitKOneKernelTokens)
+    if (T <= kSplitKOneKernelTokens && !params->batch_invariant)
         return cuda_status(launch_pre_split_k(dot_mix, sqrsum, n_splits, fa, st));
     if (mhc_status s = cuda_status(launch_coefficients_split_k(dot_mix, sqrsum, n_splits, fa, st)))
         return s;

@@ -39,7 +39,8 @@ class MhcError(RuntimeError):
 class _Params(ctypes.Structure):
     _fields_ = [("hc_norm_eps", ctypes.c_float), ("hc_pre_eps", ctypes.c_float),
                 ("hc_post_mult", ctypes.c_float), ("sinkhorn_eps", ctypes.c_float),
-                ("norm_eps", ctypes.c_float), ("sinkhorn_iters", ctypes.c_int)]
+                ("norm_eps", ctypes.c_float), ("sinkhorn_iters", ctypes.c_int),
+                ("batch_invariant", ctypes.c_int)]
 
 
 @dataclass
@@ -50,10 +51,12 @@ class Params:
     sinkhorn_eps: float = 1e-6
     norm_eps: float = 1e-6
     sinkhorn_iters: int = 20
+    batch_invariant: bool = False
 
     def c(self) -> _Params:
         return _Params(self.hc_norm_eps, self.hc_pre_eps, self.hc_post_mult,
-                       self.sinkhorn_eps, self.norm_eps, int(self.sinkhorn_iters))
+                       self.sinkhorn_eps, self.norm_eps, int(self.sinkhorn_iters),
+                       int(bool(self.batch_invariant)))
 
 
 def lib_path() -> str:
