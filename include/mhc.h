@@ -161,10 +161,11 @@ mhc_status mhc_pre(const uint16_t *residual, const void *weight, const float *sc
 /*
  * Fused post + pre boundary ("mhc_boundary" page, mhc_shifted_post_pre_boundary
  * and MhcBoundaryKernel): the residual update of mhc_post, then the pre of
- * mhc_pre computed on the UPDATED residual, in one pass over the residual.
+ * mhc_pre computed on the UPDATED residual.
  * pre_lag: [T, 4] fp32 pre of the previous boundary (shifted form: the layer
- * input collapses the updated residual with pre_lag), or NULL (unshifted
- * form: it collapses with this boundary's own pre_out).
+ * input collapses the updated residual with pre_lag, all in one pass over
+ * the residual), or NULL (unshifted form: it collapses with this boundary's
+ * own pre_out, which re-reads the updated residual).
  * Other arguments as in mhc_post and mhc_pre. residual_out may be == residual.
  */
 mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
@@ -176,10 +177,6 @@ mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
                               uint16_t *residual_out, uint16_t *layer_input,
                               float *pre_out, float *post_out, float *comb_out,
                               void *workspace, size_t workspace_bytes, void *stream);
-
-/* ---------------------------------------------------------------------- */
-/* Allocation-free variant. The pages this library follows have no          */
-/* counterpart of this entry point.                                         */
 
 /*
  * Unshifted pre from split-K mixes ("The Hyper Connection Preprocessing GPU
@@ -194,13 +191,19 @@ mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
  * RMS-normed with norm_w (or the raw collapse when norm_w is NULL).
  * n_splits in [1, 64] (the page's kernel takes 1, 2, 4, 8 or 16), else
  * MHC_ERR_SHAPE. No workspace. Outputs as in mhc_pre; none may alias an
- * input. Two kernels on `stream` (coefficients, then the collapse).
+ * input. Enqueued on `stream`: one kernel for up to 1024 tokens (the collapse
+ * overlapping the coefficients), else two (coefficients, then the collapse);
+ * always two when params->batch_invariant is set.
  */
 mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const float *sqrsum,
                            int n_splits, const float *scale, const float *base,
                            const void *norm_w, mhc_dtype norm_dtype, const mhc_params *params,
                            int64_t tokens, int hidden, uint16_t *layer_input, float *pre_out,
                            float *post_out, float *comb_out, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* Allocation-free variant. The pages this library follows have no          */
+/* counterpart of this entry point.                                         */
 
 /*
  * mhc_boundary_fused without a workspace, for callers that cannot allocate

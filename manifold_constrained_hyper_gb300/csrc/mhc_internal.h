@@ -27,8 +27,6 @@ constexpr int kStageBytes = kResBytes + kXBytes + kWBytes;
 constexpr int kPartVals = 25;
 constexpr int kTokStride = 28;
 constexpr int kItemFloats = kTileT * kTokStride;
-constexpr int kStreamThreads = 320;                 // TMA warp, MMA warp, 8 workers
-constexpr int kTmemCols = 64;
 
 struct CoefArgs {
     const float *scale;
