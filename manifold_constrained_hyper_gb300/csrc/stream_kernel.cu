@@ -45,15 +45,21 @@ constexpr int kStages = 4;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kAccBufs = 2;                            // accumulator / sums buffers
 constexpr int kLiBufs = 3;                             // shifted: collapse buffers
-constexpr int kNumBars = 3 * kStages + 4 * kAccBufs + 3 + 1;
+constexpr int kNumBars = 3 * kStages + 4 * kAccBufs + 3 + 1 + 1;
 constexpr int kSumsOff = kBarOff + 256;                // [buffers][2 halves][2 sums][128] fp32
 constexpr int kMiscOff = kSumsOff + kAccBufs * 2 * 2 * kTileT * 4;
-constexpr int kRedOff = kMiscOff + 64;                 // finisher scratch: [3][128] + [32] fp32
-constexpr int kRoundTok = 5;                           // tokens per coefficient round (<= 128 / 25)
+// scratch: the workers' coefficient reduction [256] + [128], the finishers'
+// collapse sums [128], the coefficient constants [32] (fp32)
+constexpr int kRedOff = kMiscOff + 64;
+constexpr int kWorkThreads = 256;
 constexpr int kFinThreads = 128;
+constexpr int kRoundTok = 5;                           // tokens per coefficient round
 constexpr int kFinBarrier = 1;                         // named barrier of the finisher warps
-constexpr int kSmemUsed = kRedOff + (3 * kFinThreads + 32) * 4;
-static_assert(kRoundTok * kPartVals <= kFinThreads, "one pair per finisher thread");
+constexpr int kWorkBarrier = 2;                        // named barrier of the worker warps
+constexpr int kRsumOff = kWorkThreads + kFinThreads;   // float offsets within the scratch
+constexpr int kConstOff = kRsumOff + kFinThreads;
+constexpr int kSmemUsed = kRedOff + (kConstOff + 32) * 4;
+static_assert(kRoundTok * kPartVals <= kFinThreads, "one combined value per thread");
 static_assert(kSmemUsed + 1024 <= 227 * 1024, "shared memory per CTA");
 constexpr int kAccCols = 64;                           // one accumulator buffer (48 used)
 constexpr int kLiCol = kAccBufs * kAccCols;            // shifted: collapse buffers
@@ -67,7 +73,7 @@ static_assert(128 * (kRegsProducer + kRegsFinisher) + 256 * kRegsWorker <= 65536
 enum : int { SITE_PROD_READY = 1, SITE_PROD_MMA = 2, SITE_MMA_FULL = 3, SITE_MMA_READY = 4,
              SITE_WORK_FULL = 5, SITE_FIN_ACC = 6, SITE_DRAIN = 7, SITE_MMA_ACC = 8,
              SITE_FIN_SUMS = 9, SITE_WORK_SUMS = 10, SITE_TILE_FLAGS = 11, SITE_WORK_LI = 12,
-             SITE_EXIT = 13 };
+             SITE_EXIT = 13, SITE_WORK_COEF = 14 };
 
 struct Coefs {
     uint64_t post2[4];       // (post[s], post[s])
@@ -179,6 +185,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     auto sums_empty = [&](int b) { return bars + 8u * (3 * kStages + 3 * kAccBufs + b); };
     auto li_empty = [&](int b) { return bars + 8u * (3 * kStages + 4 * kAccBufs + b); };
     const uint32_t exit_bar = bars + 8u * (3 * kStages + 4 * kAccBufs + kLiBufs);   // every warp is done
+    const uint32_t coef_go = exit_bar + 8u;   // single wave: the tile's partials are all published
     // per-token sums of squares handed from workers to finishers: [b][half][ssq, ssql][t]
     float *sums = reinterpret_cast<float *>(gbase + kSumsOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kMiscOff);
@@ -189,6 +196,25 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     const int n_local = (n_items - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x;
     const int total = n_local * d;                                   // chunks of this CTA
     const uint64_t tmo = a.timeout_ns;
+
+    // Loads of chunk g into its stage: residual and x with evict_normal
+    // (measured: evict_first on these loads cost 14 % of the call at
+    // 8192 x 7168, with the same DRAM bytes), the weight tile kept in L2.
+    const uint64_t pol_load = policy_evict_normal();
+    const uint64_t pol_keep = policy_evict_last();
+    constexpr uint32_t kLoadBytes = kResBytes + kWBytes + (MODE != PRE_ONLY ? kXBytes : 0);
+    auto issue_load = [&](int g) {
+        const int st = g % kStages;
+        const uint32_t sb = base + st * kStageBytes;
+        const Item it = item_of(g / d, n_slices);
+        const int hc = chunk_hidden(it.slice, g % d, n_slices);
+        const int t0 = it.tile * kTileT;
+        mbar_arrive_expect_tx(full(st), kLoadBytes);
+        tma_load_3d(sb, &tm_res, hc, t0, 0, full(st), pol_load);
+        if (MODE != PRE_ONLY) tma_load_2d(sb + kResBytes, &tm_x, hc, t0, full(st), pol_load);
+        bulk_load(sb + kResBytes + kXBytes, a.weight + static_cast<size_t>(hc / kChunk) * kWBytes,
+                  kWBytes, full(st), pol_keep);
+    };
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -204,8 +230,14 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         }
         for (int b = 0; b < kLiBufs; ++b) mbar_init(li_empty(b), 4);
         mbar_init(exit_bar, kThreads / 32);
+        mbar_init(coef_go, 4);
         *abort_flag = 0;
         fence_mbar_init();
+        // a single wave (a decode batch) sends its first loads before the
+        // rest of the set-up; a long run of items does better without (the
+        // 8192 x 7168 call measured 5 us slower with it)
+        if (a.fuse_coef)
+            for (int g = 0; g < total && g < kStages; ++g) issue_load(g);
     }
     constexpr uint32_t kTmemCols = MODE == FUSED_SHIFTED ? 512 : kAccBufs * kAccCols;
     static_assert(kAccBufs * kAccCols + kLiBufs * kLiCols <= 512, "TMEM columns");
@@ -229,28 +261,14 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         regs_dec_producer();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer
-            // residual and x loads: evict_normal (measured: evict_first on these
-            // loads cost 14 % of the call at 8192 x 7168, with the same DRAM bytes)
-            const uint64_t pol_load = policy_evict_normal();
+            // (in a single wave the first kStages loads went out right after
+            // the barriers were initialised)
             const uint64_t pol_stream = policy_evict_first();
-            const uint64_t pol_keep = policy_evict_last();
-            constexpr uint32_t kLoadBytes =
-                kResBytes + kWBytes + (MODE != PRE_ONLY ? kXBytes : 0);
-            auto issue_load = [&](int g) {
-                const int st = g % kStages;
-                const uint32_t sb = base + st * kStageBytes;
-                const Item it = item_of(g / d, n_slices);
-                const int hc = chunk_hidden(it.slice, g % d, n_slices);
-                const int t0 = it.tile * kTileT;
-                mbar_arrive_expect_tx(full(st), kLoadBytes);
-                tma_load_3d(sb, &tm_res, hc, t0, 0, full(st), pol_load);
-                if (MODE != PRE_ONLY) tma_load_2d(sb + kResBytes, &tm_x, hc, t0, full(st), pol_load);
-                bulk_load(sb + kResBytes + kXBytes,
-                          a.weight + static_cast<size_t>(hc / kChunk) * kWBytes, kWBytes,
-                          full(st), pol_keep);
-            };
             int loaded = 0;
-            for (; loaded < total && loaded < kStages; ++loaded) issue_load(loaded);
+            if (a.fuse_coef)
+                loaded = total < kStages ? total : kStages;
+            else
+                for (; loaded < total && loaded < kStages; ++loaded) issue_load(loaded);
             int g = 0;
             for (; g < total; ++g) {
                 const int st = g % kStages;
@@ -441,6 +459,69 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         }
         // the last item (after an abort the finishers only get their barriers)
         if (total > 0) hand_over(g < total ? g / d : n_local - 1);
+
+        // ---- one item per CTA (a single wave): once the finishers have seen
+        // every slice of the tile publish, the workers form the coefficients
+        // of the tile's tokens slice + S * j while the finishers write the
+        // layer input. In rounds of up to kRoundTok tokens the 256 worker
+        // threads split the (token, value) pairs and, when there are fewer
+        // than 256 pairs, the slices into G consecutive ranges; each thread
+        // sums its range in slice order (loads through L2 only: other CTAs
+        // wrote the partials in this kernel); one thread per pair adds the G
+        // range sums in range order; then one thread per token forms
+        // pre / post / comb. The rounds and barriers depend on the item only,
+        // so all eight worker warps take part in each.
+        if (a.fuse_coef && n_local > 0) {
+            const int wt = tid - 4 * 32;                   // 0..255 among the workers
+            const Item it = item_of(0, n_slices);
+            bool ok = mbar_wait(coef_go, 0, abort_flag, tmo, a.status, SITE_WORK_COEF);
+            ok = __all_sync(0xffffffffu, ok);
+            float *red = reinterpret_cast<float *>(gbase + kRedOff);
+            const float *consts = red + kConstOff;
+            const int ntok = it.slice < kTileT ? (kTileT - 1 - it.slice) / n_slices + 1 : 0;
+            const long long gbase_t = static_cast<long long>(it.tile) * kTileT + it.slice;
+            for (int r0 = 0; r0 < ntok; r0 += kRoundTok) {
+                int nr = ntok - r0 < kRoundTok ? ntok - r0 : kRoundTok;
+                while (nr > 0 && gbase_t + static_cast<long long>(n_slices) * (r0 + nr - 1) >= a.T) --nr;
+                const int pairs = nr * kPartVals;
+                const int G = pairs > 0 ? kWorkThreads / pairs : 1;
+                const int per = (n_slices + G - 1) / G;
+                if (ok && wt < pairs * G) {
+                    const int gi = wt / pairs, pr = wt - gi * pairs;
+                    const int j = pr / kPartVals, m = pr - j * kPartVals;
+                    const int tin = it.slice + n_slices * (r0 + j);
+                    const float *pp = a.partials + static_cast<size_t>(it.tile) * n_slices * kItemFloats +
+                                      tin * kTokStride + m;
+                    const size_t step = kItemFloats;
+                    const int s_end = (gi + 1) * per < n_slices ? (gi + 1) * per : n_slices;
+                    float sum = 0.f;
+                    for (int s2 = gi * per; s2 < s_end; s2 += 32) {
+                        float vv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) vv[i] = s2 + i < s_end ? __ldcg(pp + (s2 + i) * step) : 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (s2 + i < s_end) sum += vv[i];
+                    }
+                    red[wt] = sum;
+                }
+                named_barrier_sync(kWorkBarrier, kWorkThreads);
+                // one thread per (token, value) adds the G range sums in order
+                if (ok && wt < pairs) {
+                    float acc = 0.f;
+                    for (int gi = 0; gi < G; ++gi) acc += red[gi * pairs + wt];
+                    red[kWorkThreads + wt] = acc;
+                }
+                named_barrier_sync(kWorkBarrier, kWorkThreads);
+                if (ok && wt < nr) {
+                    const float *v = red + kWorkThreads + wt * kPartVals;
+                    coefficients_thread(v, 1, consts, a.coef, a.H,
+                                        gbase_t + static_cast<long long>(n_slices) * (r0 + wt),
+                                        a.pre_out, a.post_out, a.comb_out);
+                }
+                named_barrier_sync(kWorkBarrier, kWorkThreads);
+            }
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(exit_bar);
@@ -454,14 +535,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             a.epoch_cell != nullptr ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell)
                                     : a.epoch;
         float *red = reinterpret_cast<float *>(gbase + kRedOff);
-        float *rsum = red + 2 * kFinThreads;
-        float *consts = red + 3 * kFinThreads;
+        float *rsum = red + kRsumOff;
+        float *consts = red + kConstOff;
         stage_coef_consts(a.coef, consts, tid - 12 * 32);
         named_barrier_sync(kFinBarrier, kFinThreads);
         const int t = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint64_t pol_out = policy_evict_first();
-        const uint64_t pol_keep = policy_evict_last();
         // Item k is published as soon as its accumulator is ready; its layer
         // input is written one item later, once the tile's other slices have
         // published too (by then they almost always have).
@@ -585,6 +665,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 if (a.fuse_coef) fence_acq_rel_gpu();
                 __syncwarp();
             }
+            // the workers may form the coefficients now (also after an abort,
+            // so that their wait ends)
+            if (a.fuse_coef && lane == 0) mbar_arrive(coef_go);
             float rstd_li = 0.f;
             if (a.fuse_coef) {
                 // single wave: the four finisher warps share the reduction. The
@@ -689,63 +772,6 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(li_empty(lb));
-
-            // ---- one item per CTA (a single wave): the item also forms the
-            // coefficients of the tile's tokens slice + S * j. In rounds of up
-            // to kRoundTok tokens, the 128 finisher threads split the (token,
-            // value) pairs and, when there are fewer than 128 pairs, the slices
-            // into G consecutive groups; each thread sums its group in slice
-            // order (loads through L2 only: other CTAs wrote the partials in
-            // this kernel); one thread per pair adds the G group sums in group
-            // order; then one thread per token forms pre / post / comb. The
-            // rounds and barriers depend on the item only, so all four
-            // finisher warps take part.
-            if (a.fuse_coef) {
-                const int ntok = it.slice < kTileT ? (kTileT - 1 - it.slice) / n_slices + 1 : 0;
-                const long long gbase = static_cast<long long>(it.tile) * kTileT + it.slice;
-                const int ft = tid - 12 * 32;
-                for (int r0 = 0; r0 < ntok; r0 += kRoundTok) {
-                    int nr = ntok - r0 < kRoundTok ? ntok - r0 : kRoundTok;
-                    while (nr > 0 && gbase + static_cast<long long>(n_slices) * (r0 + nr - 1) >= a.T) --nr;
-                    const int pairs = nr * kPartVals;
-                    const int G = pairs > 0 ? kFinThreads / pairs : 1;
-                    const int per = (n_slices + G - 1) / G;
-                    if (ok && ft < pairs * G) {
-                        const int g = ft / pairs, pr = ft - g * pairs;
-                        const int j = pr / kPartVals, m = pr - j * kPartVals;
-                        const int tin = it.slice + n_slices * (r0 + j);
-                        const float *pp = a.partials + static_cast<size_t>(it.tile) * n_slices * kItemFloats +
-                                          tin * kTokStride + m;
-                        const size_t step = kItemFloats;
-                        const int s_end = (g + 1) * per < n_slices ? (g + 1) * per : n_slices;
-                        float sum = 0.f;
-                        for (int s2 = g * per; s2 < s_end; s2 += 32) {
-                            float vv[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) vv[i] = s2 + i < s_end ? __ldcg(pp + (s2 + i) * step) : 0.f;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (s2 + i < s_end) sum += vv[i];
-                        }
-                        red[ft] = sum;
-                    }
-                    named_barrier_sync(kFinBarrier, kFinThreads);
-                    // one thread per (token, value) adds the G range sums in order
-                    if (ok && ft < pairs) {
-                        float acc = 0.f;
-                        for (int g = 0; g < G; ++g) acc += red[g * pairs + ft];
-                        red[kFinThreads + ft] = acc;
-                    }
-                    named_barrier_sync(kFinBarrier, kFinThreads);
-                    if (ok && ft < nr) {
-                        const float *v = red + kFinThreads + ft * kPartVals;
-                        coefficients_thread(v, 1, consts, a.coef, a.H,
-                                            gbase + static_cast<long long>(n_slices) * (r0 + ft),
-                                            a.pre_out, a.post_out, a.comb_out);
-                    }
-                    named_barrier_sync(kFinBarrier, kFinThreads);
-                }
-            }
         }
         tc_fence_before();
         __syncwarp();
