@@ -61,7 +61,7 @@ def alg_bytes_stream_kernel(T: int, H: int) -> int:
 # workload, from one ncu capture of the current kernel
 # (profiles/boundary_prefill_t8192_h7168_dram.md); empty until the capture of
 # the current kernel is taken. None for other sizes.
-STREAM_KERNEL_TRAFFIC = {(8192, 7168): 591.65e6 + 537.41e6}
+STREAM_KERNEL_TRAFFIC = {(8192, 7168): 591.78e6 + 537.52e6}
 
 
 # ---------------------------------------------------------------- clocks
