@@ -233,6 +233,58 @@ def test_prefill_t8192_h7168_sampled_tokens():
     compare("shifted", gsel, o)
 
 
+@pytest.mark.parametrize("mode", ["shifted", "unshifted", "pre"])
+def test_large_token_count_sampled(mode):
+    """32768 tokens x hidden 7168 (1.9 GB of residual, 7168 work items, 47 per
+    CTA): offsets past 2^31 elements, checked on sampled tokens."""
+    T, H = 32768, 7168
+    d = synth.make_inputs_device(T, H, 9, "cuda")
+    rows = np.unique(np.concatenate([[0, 127, 128, 16383, 16384, T - 129, T - 128, T - 1],
+                                     np.random.default_rng(32768).integers(0, T, 24)]))
+    idx = torch.from_numpy(rows).cuda()
+    d["residual"] = host_bits(d["residual_dev"][idx])
+    d["x"] = host_bits(d["x_dev"][idx])
+    g = run_gpu(mode, d, dev_tensors={"residual": d["residual_dev"], "x": d["x_dev"]})
+    sub = dict(d, post=d["post"][rows], comb=d["comb"][rows], pre_lag=d["pre_lag"][rows])
+    o = run_oracle(mode, sub)
+    gsel = {k: (v[idx] if isinstance(v, torch.Tensor) else v) for k, v in g.items()
+            if k not in ("partials",)}
+    for k in ("pre", "post", "comb"):
+        gsel[k] = g[k][rows]
+    gsel["partials"] = g["partials"][:, rows]
+    compare(mode, gsel, o, d=sub)
+    del d, g
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode", ["shifted", "unshifted", "pre"])
+@pytest.mark.parametrize("T,H", [(1, 32), (130, 32), (3, 96), (77, 160), (129, 38912)])
+def test_hidden_size_extremes(mode, T, H):
+    """The smallest hidden (one 32-wide chunk: one slice, 128 tokens per
+    item), odd chunk counts, and the largest hidden the shifted form plans
+    with items of at most 8 chunks (152 slices of 256)."""
+    d = synth.make_inputs(T, H, seed=900 + T + H)
+    g = run_gpu(mode, d)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, d=d)
+
+
+@pytest.mark.parametrize("mode", ["unshifted", "pre"])
+def test_hidden_65536_items_of_sixteen_chunks(mode):
+    """Hidden 65536 (the largest supported): 128 slices of 16 chunks, which
+    only the unshifted forms plan (the shifted form's collapse buffer holds
+    8 chunks and the call reports MHC_ERR_UNSUPPORTED)."""
+    T, H = 5, 65536
+    d = synth.make_inputs(T, H, seed=965)
+    assert ops.plan(T, H) == (128, 512)
+    g = run_gpu(mode, d)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, d=d)
+    with pytest.raises(ops.MhcError) as e:
+        run_gpu("shifted", d)
+    assert e.value.code == 4
+
+
 # ------------------------------------------------------------------ stream capture
 
 
