@@ -284,7 +284,9 @@ __global__ void __launch_bounds__(kColThreads) collapse_unshifted_kernel(const F
     extern __shared__ uint4 li_s[];            // [H/8]
     __shared__ float red_s[kColThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const long long t = blockIdx.x;
+    // last tokens first: the streaming pass touched them last, so part of
+    // their rows is still in L2
+    const long long t = a.T - 1 - blockIdx.x;
     const float4 pv = reinterpret_cast<const float4 *>(a.pre_out)[t];
     const uint64_t p2[4] = {f2_pack(pv.x, pv.x), f2_pack(pv.y, pv.y), f2_pack(pv.z, pv.z),
                             f2_pack(pv.w, pv.w)};
