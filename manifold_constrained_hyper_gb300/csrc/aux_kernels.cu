@@ -2,6 +2,8 @@
 // of the boundary (slice reduction and coefficients; for the unshifted form
 // the collapse and its RMSNorm after them), the device status word and the
 // wait-timeout probe.
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "coef.cuh"
@@ -377,6 +379,32 @@ __global__ void unarmed_wait_kernel(unsigned int *status, unsigned long long tim
 
 }  // namespace
 
+// The dynamic shared-memory opt-in of a kernel, per device: raised to the
+// largest size asked for so far (H * 2 bytes for the collapse kernels, up to
+// 128 KB), so that a run of calls pays for it once.
+struct SmemOptIn {
+    std::atomic<int> bytes[64];
+};
+
+template <typename K>
+cudaError_t ensure_dynamic_smem(K kernel, SmemOptIn &opt, size_t smem) {
+    if (smem <= 48 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::atomic<int> &cur = opt.bytes[dev & 63];
+    if (cur.load(std::memory_order_acquire) >= static_cast<int>(smem)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int prev = cur.load();
+    while (prev < static_cast<int>(smem) && !cur.compare_exchange_weak(prev, static_cast<int>(smem))) {
+    }
+    return cudaSuccess;
+}
+
+SmemOptIn g_optin_split_k, g_optin_collapse;
+
 unsigned int *device_status_word() {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
@@ -425,12 +453,7 @@ cudaError_t launch_coefficients_split_k(const float *dot_mix, const float *sqrsu
 cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
                                const FinishArgs &a, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(a.H) * 2;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(pre_split_k_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
+    if (cudaError_t e = ensure_dynamic_smem(pre_split_k_kernel, g_optin_split_k, smem)) return e;
     pre_split_k_kernel<<<static_cast<unsigned>(a.T), kSkThreads, smem, s>>>(dot_mix, sqrsum,
                                                                           n_splits, a);
     return cudaGetLastError();
@@ -438,12 +461,8 @@ cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_
 
 cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s) {
     const size_t smem = static_cast<size_t>(a.H) * 2;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(collapse_unshifted_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
+    if (cudaError_t e = ensure_dynamic_smem(collapse_unshifted_kernel, g_optin_collapse, smem))
+        return e;
     collapse_unshifted_kernel<<<static_cast<unsigned>(a.T), kColThreads, smem, s>>>(a);
     return cudaGetLastError();
 }

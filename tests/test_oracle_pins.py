@@ -468,3 +468,29 @@ def test_split_k_single_split_rstd_and_coefficients():
     want = _bf16(acc)
     diff = np.abs(out["layer_input"].astype(np.int32) - want.astype(np.int32))
     assert diff.max() <= 1          # numpy's separately rounded multiply-add vs the fma chain
+
+
+# ---------------------------------------------------------------- regression fixture
+
+
+def test_oracle_reproduces_the_golden_fixture():
+    """tests/golden/tiny_t4_h256_shifted.txt (written by make_golden.py from
+    the oracle itself): a regression pin, bit for bit."""
+    import os
+    import importlib.util
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location("make_golden", os.path.join(here, "make_golden.py"))
+    mg = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mg)
+    want = {}
+    with open(os.path.join(here, "tiny_t4_h256_shifted.txt")) as f:
+        lines = [l.rstrip("\n") for l in f if not l.startswith("#")]
+    for head, body in zip(lines[0::2], lines[1::2]):
+        name, dtype, *shape = head.split()
+        bits = np.array([int(b, 16) for b in body.split()],
+                        np.uint16 if dtype == "uint16" else np.uint32)
+        want[name] = bits.view(np.dtype(dtype)).reshape([int(s) for s in shape])
+    got = mg.oracle_outputs()
+    assert set(got) == set(want)
+    for k in got:
+        assert np.array_equal(got[k].view(np.uint8), np.ascontiguousarray(want[k]).view(np.uint8)), k
