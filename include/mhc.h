@@ -264,9 +264,10 @@ mhc_status mhc_debug_unarmed_wait(void *stream);
 
 /* Benchmark hook: the next mhc_pre / mhc_boundary_fused call made by this
  * host thread records `event` (a cudaEvent_t passed as void*) on its stream
- * right after its streaming kernel and before its finishing kernel, so that
- * the two kernels can be timed apart with events. Consumed by that call;
- * NULL clears a pending event. */
+ * right after its streaming kernel and before its finishing kernel (the
+ * unshifted forms), so that the two kernels can be timed apart with events;
+ * a shifted call is the streaming kernel alone, and the event follows it.
+ * Consumed by that call; NULL clears a pending event. */
 void mhc_debug_record_between(void *event);
 
 /* Test hook for the coefficients' reciprocal (the "mhc_boundary" page's rcp:

@@ -167,7 +167,7 @@ void plan(long long T, int H, int *n_slices, int *slice_w) {
     *slice_w = best_d * kChunk;
 }
 
-// Workspace: per-item partial blocks [tiles][S] of 128 x 28 fp32, then (each 256-byte
+// Workspace: per-item partial blocks [tiles][S] of 128 x 32 fp32, then (each 256-byte
 // aligned) the shifted form's per-slice collapse sums [S][T] fp32, its
 // publication flags [tiles][S][4] u64, and the u64 epoch cell that a call
 // being captured into a CUDA graph takes its flag value from.
@@ -225,14 +225,15 @@ bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T) {
 }
 
 // Tensor maps of the last few calls of this host thread, by (kind, pointer,
-// H, T): a decode loop reuses its buffers, and encoding costs host time.
+// H, T) (kind 0 residual-shaped, 1 x-shaped): a decode loop reuses its
+// buffers, and encoding costs host time.
 struct MapCache {
     struct Entry {
         int kind = -1, H = 0;
         long long T = 0;
         const void *ptr = nullptr;
         CUtensorMap map;
-    } e[6];
+    } e[8];
     int next = 0;
 };
 thread_local MapCache t_maps;
@@ -247,7 +248,7 @@ bool encode_cached(int kind, CUtensorMap *m, const void *ptr, int H, long long T
     const bool ok = kind == 0 ? encode_res(m, ptr, H, T) : encode_2d(m, ptr, H, T);
     if (ok) {
         auto &x = t_maps.e[t_maps.next];
-        t_maps.next = (t_maps.next + 1) % 6;
+        t_maps.next = (t_maps.next + 1) % 8;
         x.kind = kind;
         x.ptr = ptr;
         x.H = H;
@@ -382,9 +383,13 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // the shifted form finishes in-kernel: every slice of a tile must be in
     // flight at once, and an item's collapse must fit its TMEM buffer
     if (mode == FUSED_SHIFTED && (S > grid || w / kChunk > 8)) return MHC_ERR_UNSUPPORTED;
-    // a single wave of items: the shifted form's finishers form the
-    // coefficients too (no second kernel)
+    // the shifted form forms the coefficients in the streaming kernel, by
+    // its workers: in a single wave of items as soon as the tile has
+    // published (reduction split into ranges, for latency), otherwise after
+    // the CTA's last item (reduction in slice order, as in the
+    // batch-invariant plan)
     sa.fuse_coef = mode == FUSED_SHIFTED && items <= grid && !invariant;
+    sa.coef_end = mode == FUSED_SHIFTED && !sa.fuse_coef;
     if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, sa, S,
                                                  static_cast<int>(items), grid, st)))
         return s;
@@ -407,9 +412,8 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     fa.comb_out = comb_out;
     fa.T = T;
     fa.H = H;
-    if (sa.fuse_coef) return MHC_OK;
-    if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
     if (mode == FUSED_SHIFTED) return MHC_OK;
+    if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
     return cuda_status(launch_collapse_unshifted(fa, st));
 }
 

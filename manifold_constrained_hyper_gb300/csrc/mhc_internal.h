@@ -21,12 +21,16 @@ constexpr int kStageBytes = kResBytes + kXBytes + kWBytes;
 // Partials of one (tile, slice) item, a block of kItemFloats fp32: per token,
 // values 0-23 the partial mixes (hi + lo), 24 the partial 4H sum of squares.
 // Value-major [kPartVals][kTileT] (a warp reads or writes one value of 32
-// tokens as one 128-byte row) when a separate kernel reduces them;
-// token-major [kTileT][kTokStride] (16-byte aligned runs) when the streaming
-// kernel's finishers reduce them for a few tokens each (a single wave).
+// tokens as one 128-byte row) in general; token-major [kTileT][kTokStride]
+// (16-byte aligned runs) when the call is a single wave of items and the
+// shifted streaming kernel's workers reduce them for a few tokens each.
+// Multi-item shifted calls use a third layout: per token a 32-float record
+// for each slice, [T rounded up to tiles][S][kRecFloats] (a 4-token group's
+// records of every slice are one contiguous run, fetched by one bulk copy).
 constexpr int kPartVals = 25;
 constexpr int kTokStride = 28;
-constexpr int kItemFloats = kTileT * kTokStride;
+constexpr int kRecFloats = 32;
+constexpr int kItemFloats = kTileT * kRecFloats;    // one item's share of the workspace
 
 struct CoefArgs {
     const float *scale;
@@ -57,7 +61,9 @@ struct StreamArgs {
     int out32;                   // layer_input 32-byte aligned
     uint16_t *layer_input;       // [T,H]
     float *pre_out, *post_out, *comb_out;
-    int fuse_coef;               // one item per CTA: the finishers also form the coefficients
+    int fuse_coef;               // one item per CTA: the workers form the coefficients
+    int coef_end;                // shifted, several items per CTA: the workers form
+                                 // them after the CTA's last item (record layout)
 };
 
 struct FinishArgs {

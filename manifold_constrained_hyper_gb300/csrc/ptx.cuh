@@ -272,6 +272,12 @@ __device__ __forceinline__ unsigned long long flag_relaxed(const unsigned long l
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
+// Orders this thread's view of global memory written through the generic
+// proxy (other threads' plain stores it has acquired) before its following
+// async-proxy (TMA) reads of that memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void fence_acq_rel_gpu() {
     asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }

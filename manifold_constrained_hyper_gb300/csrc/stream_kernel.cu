@@ -21,16 +21,21 @@
 // workers also collapse the updated residual with the lagged pre into TMEM;
 // the finishers publish the item with a per-call flag, wait until every
 // slice of the tile has published, and write the layer input
-// bf16((li * rsqrt(sum li^2 / H + eps)) * norm_w) from TMEM. When every CTA
-// has a single item (a decode batch) the finishers then also form the
-// coefficients; otherwise a small kernel forms them from the partials.
+// bf16((li * rsqrt(sum li^2 / H + eps)) * norm_w) from TMEM. The shifted form
+// also forms the coefficients in this kernel, by its worker warps: when every
+// CTA has a single item (a decode batch) as soon as the tile has published;
+// otherwise once the CTA has streamed its last chunk, from partial records
+// that bulk copies land in the then idle stage buffers (nothing of it runs
+// while the CTA streams). The other forms leave the coefficients to a small
+// kernel that reduces the partials.
 //
 // Warps: 0 TMA producer and TMEM owner, 1 MMA issuer, 2-3 idle, 4-11
 // workers (token 32*(warp%4) + lane, so a warp's tokens are its TMEM lane
 // quarter; warps 4-7 take hidden 0-15 of a chunk, 8-11 hidden 16-31), 12-15
 // finishers (token 32*(warp%4) + lane). Registers are redistributed per
 // warpgroup with setmaxnreg: 40 + 184 + 184 + 96 per thread, 64,512 of the
-// 65,536 the CTA is launched with.
+// 65,536 the CTA is launched with (the workers measured 2 % slower at 168,
+// the finishers 3 % at 88).
 #include <atomic>
 
 #include "coef.cuh"
@@ -45,8 +50,9 @@ constexpr int kStages = 4;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kAccBufs = 2;                            // accumulator / sums buffers
 constexpr int kLiBufs = 3;                             // shifted: collapse buffers
-constexpr int kNumBars = 3 * kStages + 4 * kAccBufs + 3 + 1 + 1;
-constexpr int kSumsOff = kBarOff + 256;                // [buffers][2 halves][2 sums][128] fp32
+constexpr int kNumBars = 3 * kStages + 4 * kAccBufs + 3 + 1 + 1 + 4;
+constexpr int kBarBytes = 256;
+constexpr int kSumsOff = kBarOff + kBarBytes;          // [buffers][2 halves][2 sums][128] fp32
 constexpr int kMiscOff = kSumsOff + kAccBufs * 2 * 2 * kTileT * 4;
 // scratch: the workers' coefficient reduction [256] + [128], the finishers'
 // collapse sums [128], the coefficient constants [32] (fp32)
@@ -59,15 +65,21 @@ constexpr int kWorkBarrier = 2;                        // named barrier of the w
 constexpr int kRsumOff = kWorkThreads + kFinThreads;   // float offsets within the scratch
 constexpr int kConstOff = kRsumOff + kFinThreads;
 constexpr int kSmemUsed = kRedOff + (kConstOff + 32) * 4;
+// shifted, several items per CTA: the coefficients are formed after the
+// CTA's last item, from token groups' partial records [4][S][32] fp32 landed
+// by bulk copies in the (then free) stage buffers
+constexpr int kCoefGroup = 4;                          // tokens per group
+constexpr int kCoefPairs = kCoefGroup * kPartVals;     // (token, value) pairs of a group
+constexpr int kEndGroups = kWorkThreads / kCoefGroup;  // token groups per round at most
 static_assert(kRoundTok * kPartVals <= kFinThreads, "one combined value per thread");
 static_assert(kSmemUsed + 1024 <= 227 * 1024, "shared memory per CTA");
 constexpr int kAccCols = 64;                           // one accumulator buffer (48 used)
 constexpr int kLiCol = kAccBufs * kAccCols;            // shifted: collapse buffers
 constexpr int kLiCols = 128;                           // 8 chunks x 16 columns
 constexpr int kRegsProducer = 40, kRegsWorker = 184, kRegsFinisher = 96;
-static_assert(kNumBars * 8 <= 256, "barrier area");
-static_assert(128 * (kRegsProducer + kRegsFinisher) + 256 * kRegsWorker <= 65536,
-              "register split exceeds the CTA's allocation");
+static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
+static_assert(128 * (kRegsProducer + kRegsFinisher) + 256 * kRegsWorker <= kThreads * 128,
+              "register split exceeds the CTA's allocation (512 threads x 128 at launch)");
 
 // Wait-site ids recorded with a timeout.
 enum : int { SITE_PROD_READY = 1, SITE_PROD_MMA = 2, SITE_MMA_FULL = 3, SITE_MMA_READY = 4,
@@ -142,10 +154,10 @@ __device__ __forceinline__ void regs_dec_finisher() {
 
 // Bounded wait that ignores the abort flag (drains copies in flight before
 // the CTA exits after an abort).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                            unsigned int *status) {
     int local = 0;
-    mbar_wait(bar, parity, &local, timeout_ns, status, SITE_DRAIN);
+    return mbar_wait(bar, parity, &local, timeout_ns, status, SITE_DRAIN);
 }
 
 // Work item k of this CTA -> (tile, slice). Consecutive CTAs take the
@@ -186,6 +198,14 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     auto li_empty = [&](int b) { return bars + 8u * (3 * kStages + 4 * kAccBufs + b); };
     const uint32_t exit_bar = bars + 8u * (3 * kStages + 4 * kAccBufs + kLiBufs);   // every warp is done
     const uint32_t coef_go = exit_bar + 8u;   // single wave: the tile's partials are all published
+    // several items: the producer's copies have left the stage buffers;
+    // every finisher warp has seen the tile of the CTA's last item but one
+    // (prev_go) and of its last item (end_go) published; a round's partial
+    // records have landed (end_full)
+    const uint32_t stages_free = coef_go + 8u;
+    const uint32_t prev_go = stages_free + 8u;
+    const uint32_t end_go = prev_go + 8u;
+    const uint32_t end_full = end_go + 8u;
     // per-token sums of squares handed from workers to finishers: [b][half][ssq, ssql][t]
     float *sums = reinterpret_cast<float *>(gbase + kSumsOff);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kMiscOff);
@@ -231,6 +251,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         for (int b = 0; b < kLiBufs; ++b) mbar_init(li_empty(b), 4);
         mbar_init(exit_bar, kThreads / 32);
         mbar_init(coef_go, 4);
+        mbar_init(stages_free, 1);
+        mbar_init(prev_go, 4);
+        mbar_init(end_go, 4);
+        mbar_init(end_full, 1);
         *abort_flag = 0;
         fence_mbar_init();
         // a single wave (a decode batch) sends its first loads before the
@@ -298,6 +322,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 for (int c = g; c < loaded; ++c)
                     drain_wait(full(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
+            // the stage buffers are free of this CTA's copies
+            if (MODE == FUSED_SHIFTED && a.coef_end) mbar_arrive(stages_free);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
@@ -460,6 +486,99 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // the last item (after an abort the finishers only get their barriers)
         if (total > 0) hand_over(g < total ? g / d : n_local - 1);
 
+        // ---- several items per CTA: the coefficients of every token of the
+        // CTA's items, formed by the workers once they have streamed their
+        // last chunk and the producer's copies have left the stage buffers
+        // (free from then on): first those of items 0..n-2, whose tiles have
+        // long published by then (prev_go), then those of the last item once
+        // its tile has too (end_go), so that little is left for the end of
+        // the kernel. Nothing of this runs while the CTA streams. Token groups
+        // of 4 (tokens 4gi..4gi+3 of an item's tile, gi = slice, slice + S,
+        // ...) go in rounds of up to kEndGroups: one bulk copy per group lands
+        // its partial records [4 tokens][S slices][32] (contiguous in the
+        // workspace) in its slot of the stage area, all in flight at once; a
+        // thread per (group, token, value) sums over the slices in slice
+        // order (a running sum from zero, as every other path) and leaves the
+        // sum in place; then a thread per token forms pre / post / comb.
+        // Worker thread 0 lays out each round in shared memory, so every
+        // worker warp takes part in each barrier, also after an abort.
+        if (MODE == FUSED_SHIFTED && a.coef_end) {
+            const int wt = tid - 4 * 32;                   // 0..255 among the workers
+            bool ok = g == total && mbar_wait(stages_free, 0, abort_flag, tmo, a.status, SITE_WORK_COEF);
+            ok = __all_sync(0xffffffffu, ok);
+            int *rdesc = reinterpret_cast<int *>(gbase + kRedOff);   // count, then (tile, group)
+            const float *consts = reinterpret_cast<const float *>(gbase + kRedOff) + kConstOff;
+            const uint32_t grp_bytes = kCoefGroup * n_slices * kRecFloats * 4;
+            const uint32_t slot = (grp_bytes + 127u) & ~127u;
+            int per_round = static_cast<int>((kStages * kStageBytes) / slot);
+            if (per_round > kEndGroups) per_round = kEndGroups;
+            const uint64_t pol_once = policy_evict_first();
+            int ck = 0, cg = item_of(0, n_slices).slice;   // thread 0: next (item, group)
+            uint32_t round = 0;
+            for (int phase = 0; phase < 2; ++phase) {
+                // phase 0: items [0, n_local - 1); phase 1: the last item
+                const int k_end = phase == 0 ? n_local - 1 : n_local;
+                if (phase == 0 && k_end <= 0) continue;
+                const uint32_t go = phase == 0 ? prev_go : end_go;
+                ok = __all_sync(0xffffffffu, ok && mbar_wait(go, 0, abort_flag, tmo, a.status, SITE_WORK_COEF));
+                for (;; ++round) {
+                    if (wt == 0) {
+                        int n = 0;
+                        while (ok && n < per_round && ck < k_end) {
+                            const Item it = item_of(ck, n_slices);
+                            if (cg < kTileT / kCoefGroup &&
+                                static_cast<long long>(it.tile) * kTileT + kCoefGroup * cg < a.T) {
+                                rdesc[1 + 2 * n] = it.tile;
+                                rdesc[2 + 2 * n] = cg;
+                                ++n;
+                                cg += n_slices;
+                            } else if (++ck < n_local) {
+                                cg = item_of(ck, n_slices).slice;
+                            }
+                        }
+                        rdesc[0] = n;
+                        if (n > 0) mbar_arrive_expect_tx(end_full, n * grp_bytes);
+                    }
+                    named_barrier_sync(kWorkBarrier, kWorkThreads);
+                    const int n = rdesc[0];
+                    named_barrier_sync(kWorkBarrier, kWorkThreads);   // rdesc[0] read by all
+                    if (n == 0) break;
+                    if (wt < n) {
+                        // the records were written by other CTAs' generic
+                        // stores, acquired through the finishers (prev_go, end_go)
+                        const long long t0 = static_cast<long long>(rdesc[1 + 2 * wt]) * kTileT +
+                                             kCoefGroup * rdesc[2 + 2 * wt];
+                        fence_proxy_async_global();
+                        bulk_load(base + wt * slot, a.partials + t0 * n_slices * kRecFloats, grp_bytes,
+                                  end_full, pol_once);
+                    }
+                    // the copies must land before the buffers are read or the
+                    // CTA exits: a bounded wait that ignores aborts
+                    drain_wait(end_full, round & 1, tmo, a.status);
+                    for (int pr = wt; pr < n * kCoefPairs; pr += kWorkThreads) {
+                        const int i = pr / kCoefPairs, r = pr - i * kCoefPairs;
+                        const int q = r / kPartVals, m = r - q * kPartVals;
+                        float *v = reinterpret_cast<float *>(gbase + i * slot) + q * n_slices * kRecFloats + m;
+                        float acc = 0.f;
+                        for (int s2 = 0; s2 < n_slices; ++s2) acc += v[s2 * kRecFloats];
+                        v[0] = acc;                        // the token's value m, in place
+                    }
+                    named_barrier_sync(kWorkBarrier, kWorkThreads);
+                    if (ok && wt < n * kCoefGroup) {
+                        const int i = wt / kCoefGroup, q = wt - i * kCoefGroup;
+                        const long long tok = static_cast<long long>(rdesc[1 + 2 * i]) * kTileT +
+                                              kCoefGroup * rdesc[2 + 2 * i] + q;
+                        if (tok < a.T)
+                            coefficients_thread(reinterpret_cast<const float *>(gbase + i * slot) +
+                                                    q * n_slices * kRecFloats,
+                                                1, consts, a.coef, a.H, tok, a.pre_out, a.post_out,
+                                                a.comb_out);
+                    }
+                    named_barrier_sync(kWorkBarrier, kWorkThreads);
+                }
+            }
+        }
+
         // ---- one item per CTA (a single wave): once the finishers have seen
         // every slice of the tile publish, the workers form the coefficients
         // of the tile's tokens slice + S * j while the finishers write the
@@ -576,8 +695,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     float *rec = a.partials +
                                  (static_cast<size_t>(it.tile) * n_slices + it.slice) * kItemFloats;
                     if (a.fuse_coef) {
-                        // token-major [128][28]: the finishers of this kernel
-                        // read a token's 25 values as one contiguous run
+                        // token-major [128][28]: the workers of this CTA and the
+                        // tile's other CTAs read a token's 25 values as one run
                         float4 *dst = reinterpret_cast<float4 *>(rec + t * kTokStride);
                         float o[kTokStride];
 #pragma unroll
@@ -587,6 +706,23 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
 #pragma unroll
                         for (int i = 0; i < kTokStride / 4; ++i)
                             dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    } else if (MODE == FUSED_SHIFTED) {
+                        // the token's 128-byte record of this slice: four 32-byte
+                        // stores of whole sectors, kept in L2 for the end of the
+                        // kernel (where a token group's records of every slice
+                        // are one contiguous run)
+                        float *dst = a.partials + (gt * n_slices + it.slice) * kRecFloats;
+                        uint32_t o[kRecFloats];
+#pragma unroll
+                        for (int i = 0; i < 24; ++i) o[i] = __float_as_uint(__uint_as_float(v[i]) + __uint_as_float(v[24 + i]));
+                        o[24] = __float_as_uint(ssq);
+#pragma unroll
+                        for (int i = 25; i < kRecFloats; ++i) o[i] = 0u;
+#pragma unroll
+                        for (int i = 0; i < kRecFloats / 8; ++i)
+                            st_global_v8(dst + 8 * i, make_uint4(o[8 * i], o[8 * i + 1], o[8 * i + 2], o[8 * i + 3]),
+                                         make_uint4(o[8 * i + 4], o[8 * i + 5], o[8 * i + 6], o[8 * i + 7]),
+                                         pol_keep);
                     } else {
                         // value-major [25][128], kept in L2 for the kernel that
                         // reduces them next: a warp writes 128-byte rows
@@ -627,7 +763,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             // slice, spread over the lanes. Forming the coefficients here
             // needs every quarter's flags: relaxed reads, all in flight, then
             // one acquire fence once the warp has seen them all.
-            if (ok && (a.norm_w != nullptr || a.fuse_coef)) {
+            if (ok && (a.norm_w != nullptr || a.fuse_coef || a.coef_end)) {
                 const unsigned long long *fl = a.flags + static_cast<long long>(it.tile) * n_slices * 4;
                 const int nf = n_slices;
                 uint64_t t_start = 0;
@@ -664,6 +800,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 }
                 if (a.fuse_coef) fence_acq_rel_gpu();
                 __syncwarp();
+                // the tiles of items 0..kn have all published in full (each
+                // finisher warp saw its quarter of each): the workers may form
+                // their coefficients (all but the last item's, then the last)
+                if (a.coef_end && kn >= n_local - 2 && ok && lane == 0)
+                    mbar_arrive(kn == n_local - 1 ? end_go : prev_go);
             }
             // the workers may form the coefficients now (also after an abort,
             // so that their wait ends)

@@ -109,12 +109,27 @@ def test_ragged_tiles(mode, T, H):
 def test_slice_plans_at_hidden_7168(mode, T):
     """Token counts whose plans differ at hidden 7168: 56 slices of 128 over
     two tiles, 32 slices of 224 over three tiles with a ragged tail (both a
-    single wave: coefficients formed in the streaming kernel), and 32 slices
-    over eight tiles (two items per CTA: coefficients kernel)."""
+    single wave), and 32 slices over eight tiles (two items per CTA). The
+    shifted form forms the coefficients in the streaming kernel in every
+    case; the others in a second kernel."""
     d = synth.make_inputs(T, 7168, seed=500 + T)
     g = run_gpu(mode, d)
     o = run_oracle(mode, d)
     compare(mode, g, o, d=d)
+
+
+@pytest.mark.parametrize("T,H", [(1301, 7168), (5000, 1024), (3001, 2048)])
+def test_shifted_several_items_per_cta(T, H):
+    """Shifted calls with several items per CTA, whose coefficients are formed
+    by the streaming kernel's coefficient warps from 4-token groups: more
+    than 28 slices (two copies per group) with a ragged last group, 8 slices
+    (four groups per slice) and 16 slices with a ragged last group."""
+    S, _ = ops.plan(T, H)
+    assert (T + 127) // 128 * S > 152
+    d = synth.make_inputs(T, H, seed=700 + T)
+    g = run_gpu("shifted", d)
+    o = run_oracle("shifted", d)
+    compare("shifted", g, o, d=d)
 
 
 @pytest.mark.parametrize("mode", ["pre", "unshifted", "shifted"])
