@@ -199,11 +199,17 @@ size_t workspace_bytes(long long T, int H) {
     return a > b ? a : b;
 }
 
+// Token rows per box: a call of one tile loads only the rows it has (rounded
+// up to 8), one box per stream; larger calls take whole 128-row tiles of all
+// four streams in one box (box_rows 0).
+int box_rows_for(long long T) { return T <= kTileT ? static_cast<int>((T + 7) / 8 * 8) : 0; }
+
 // bf16 [rows.., H] viewed by TMA: dim0 = hidden (box 32, 64-byte swizzle).
 bool encode_2d(CUtensorMap *m, const void *ptr, int H, long long T) {
+    const int br = box_rows_for(T);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * 2};
-    cuuint32_t box[2] = {kChunk, kTileT};
+    cuuint32_t box[2] = {kChunk, static_cast<cuuint32_t>(br ? br : kTileT)};
     cuuint32_t estr[2] = {1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -212,11 +218,13 @@ bool encode_2d(CUtensorMap *m, const void *ptr, int H, long long T) {
 }
 
 // bf16 [T, 4, H] viewed as (hidden, token, stream) so that a box lands in
-// shared memory as [stream][token][32 hidden].
+// shared memory as [stream][token][32 hidden] (one stream per box when the
+// call is a single tile).
 bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T) {
+    const int br = box_rows_for(T);
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T), 4};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * 8, static_cast<cuuint64_t>(H) * 2};
-    cuuint32_t box[3] = {kChunk, kTileT, 4};
+    cuuint32_t box[3] = {kChunk, static_cast<cuuint32_t>(br ? br : kTileT), br ? 1u : 4u};
     cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -371,6 +379,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.norm_w = norm_w;
     sa.nw_bf16 = norm_dtype == MHC_BF16;
     sa.out32 = (reinterpret_cast<uintptr_t>(layer_input) & 31u) == 0;
+    sa.box_rows = box_rows_for(T);
     sa.layer_input = layer_input;
     sa.pre_out = pre_out;
     sa.post_out = post_out;

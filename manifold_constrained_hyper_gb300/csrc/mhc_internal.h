@@ -64,6 +64,8 @@ struct StreamArgs {
     int fuse_coef;               // one item per CTA: the workers form the coefficients
     int coef_end;                // shifted, several items per CTA: the workers form
                                  // them after the CTA's last item (record layout)
+    int box_rows;                // one tile: token rows per residual / x box (the
+                                 // residual maps then hold one stream per box); 0: 128
 };
 
 struct FinishArgs {

@@ -223,14 +223,29 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     const uint64_t pol_load = policy_evict_normal();
     const uint64_t pol_keep = policy_evict_last();
     constexpr uint32_t kLoadBytes = kResBytes + kWBytes + (MODE != PRE_ONLY ? kXBytes : 0);
+    // A call of one tile (box_rows != 0) loads only the first box_rows token
+    // rows of each stream, one box per stream into the same place of the
+    // stage: the copy engine spends time on every row of a box, filled or
+    // not, and a decode batch has few tokens. Rows past box_rows keep stale
+    // contents; they belong to tokens >= T, whose results are never used.
+    const int box_rows = a.box_rows;
+    const uint32_t load_bytes =
+        box_rows == 0 ? kLoadBytes
+                      : kWBytes + (MODE != PRE_ONLY ? 5u : 4u) * static_cast<uint32_t>(box_rows) * kRowBytes;
     auto issue_load = [&](int g) {
         const int st = g % kStages;
         const uint32_t sb = base + st * kStageBytes;
         const Item it = item_of(g / d, n_slices);
         const int hc = chunk_hidden(it.slice, g % d, n_slices);
         const int t0 = it.tile * kTileT;
-        mbar_arrive_expect_tx(full(st), kLoadBytes);
-        tma_load_3d(sb, &tm_res, hc, t0, 0, full(st), pol_load);
+        mbar_arrive_expect_tx(full(st), load_bytes);
+        if (box_rows == 0) {
+            tma_load_3d(sb, &tm_res, hc, t0, 0, full(st), pol_load);
+        } else {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                tma_load_3d(sb + s * kTileT * kRowBytes, &tm_res, hc, t0, s, full(st), pol_load);
+        }
         if (MODE != PRE_ONLY) tma_load_2d(sb + kResBytes, &tm_x, hc, t0, full(st), pol_load);
         bulk_load(sb + kResBytes + kXBytes, a.weight + static_cast<size_t>(hc / kChunk) * kWBytes,
                   kWBytes, full(st), pol_keep);
@@ -302,7 +317,14 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     const uint32_t sb = base + st * kStageBytes;
                     const Item it = item_of(g / d, n_slices);
                     const int hc = chunk_hidden(it.slice, g % d, n_slices);
-                    tma_store_3d(&tm_rout, hc, it.tile * kTileT, 0, sb, pol_stream);
+                    if (box_rows == 0) {
+                        tma_store_3d(&tm_rout, hc, it.tile * kTileT, 0, sb, pol_stream);
+                    } else {
+#pragma unroll
+                        for (int s = 0; s < 4; ++s)
+                            tma_store_3d(&tm_rout, hc, it.tile * kTileT, s, sb + s * kTileT * kRowBytes,
+                                         pol_stream);
+                    }
                     bulk_commit();
                 }
                 // refill the stage of the previous chunk: its store has had a
@@ -767,7 +789,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 const unsigned long long *fl = a.flags + static_cast<long long>(it.tile) * n_slices * 4;
                 const int nf = n_slices;
                 uint64_t t_start = 0;
-                while (true) {
+                // a single wave: warp 0 alone polls (every flag of the tile),
+                // then hands the result to the other finisher warps through a
+                // named barrier (fewer loads on the tile's few flag lines)
+                while (!a.fuse_coef || q == 0) {
                     bool seen = true;
                     if (a.fuse_coef) {
                         for (int f0 = lane; f0 < nf; f0 += 32 * 8) {
@@ -796,15 +821,22 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                         ok = false;
                         break;
                     }
-                    nanosleep_ns(a.fuse_coef ? 64 : 256);
+                    if (!a.fuse_coef) nanosleep_ns(256);
                 }
-                if (a.fuse_coef) fence_acq_rel_gpu();
+                if (a.fuse_coef && q == 0) fence_acq_rel_gpu();
                 __syncwarp();
                 // the tiles of items 0..kn have all published in full (each
                 // finisher warp saw its quarter of each): the workers may form
                 // their coefficients (all but the last item's, then the last)
                 if (a.coef_end && kn >= n_local - 2 && ok && lane == 0)
                     mbar_arrive(kn == n_local - 1 ? end_go : prev_go);
+            }
+            if (a.fuse_coef) {
+                // warp 0's verdict, and (through the barrier) what it acquired
+                volatile int *fin_ok = reinterpret_cast<volatile int *>(gbase + kMiscOff + 32);
+                if (q == 0 && lane == 0) *fin_ok = ok ? 1 : 0;
+                named_barrier_sync(kFinBarrier, kFinThreads);
+                ok = ok && *fin_ok != 0;
             }
             // the workers may form the coefficients now (also after an abort,
             // so that their wait ends)
@@ -830,7 +862,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     for (int s2 = sg * per; s2 < s_end; s2 += 32) {
                         float vv[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) vv[i] = s2 + i < s_end ? pp[(s2 + i) * step] : 0.f;
+                        for (int i = 0; i < 32; ++i) vv[i] = s2 + i < s_end ? __ldcg(pp + (s2 + i) * step) : 0.f;
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
                             if (s2 + i < s_end) part += vv[i];
@@ -851,7 +883,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 for (int s2 = 0; s2 < n_slices; s2 += 32) {
                     float vv[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) vv[i] = s2 + i < n_slices ? pp[(s2 + i) * step] : 0.f;
+                    for (int i = 0; i < 32; ++i) vv[i] = s2 + i < n_slices ? __ldcg(pp + (s2 + i) * step) : 0.f;
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         if (s2 + i < n_slices) sl += vv[i];
