@@ -281,6 +281,18 @@ void mhc_debug_record_between(void *event);
 mhc_status mhc_debug_rcp_check(uint32_t first_bits, uint64_t count, unsigned long long *result,
                                void *stream);
 
+/* Test hook for the two forms of the coefficients: from reduced values
+ * values [tokens][25] fp32 (24 mixes, then the 4H sum of squares), forms
+ * pre / post / comb once with one thread per token and once with 16 lanes
+ * per token (the form a single-wave shifted call uses), into out_thread and
+ * out_lanes [tokens][24] fp32 (pre 4, post 4, comb 16). The two must be
+ * bitwise equal. scale [3], base [24] and params as in mhc_pre; device
+ * pointers, 16-byte aligned; outputs must not overlap the inputs or each
+ * other. Enqueued on `stream`. The pages have no counterpart. */
+mhc_status mhc_debug_coef_check(const float *values, const float *scale, const float *base,
+                                const mhc_params *params, int hidden, int64_t tokens,
+                                float *out_thread, float *out_lanes, void *stream);
+
 /* Slice plan chosen for (T, H): writes the number of hidden slices and the
  * slice width. For tests and the benchmark's byte accounting. */
 mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width);

@@ -472,6 +472,40 @@ cudaError_t launch_epoch_bump(unsigned long long *cell, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Test hook: the coefficients of n tokens from reduced values v [n][25],
+// formed once by coefficients_thread (one thread per token) and once by
+// coefficients_16lanes (16 lanes per token), into two sets of outputs
+// [n][24] (pre 4, post 4, comb 16). 32 tokens per block of 32 threads.
+__global__ void coef_check_kernel(const float *__restrict__ v, CoefArgs c, int H, long long n,
+                                  float *out_thread, float *out_lanes) {
+    __shared__ float sb[32];
+    __shared__ float vs[32 * kPartVals];
+    const int lane = threadIdx.x;
+    const long long t0 = static_cast<long long>(blockIdx.x) * 32;
+    stage_coef_consts(c, sb, lane);
+    for (int i = lane; i < 32 * kPartVals; i += 32)
+        vs[i] = t0 * kPartVals + i < n * kPartVals ? v[t0 * kPartVals + i] : 1.f;
+    __syncwarp();
+    const long long t = t0 + lane;
+    if (t < n)
+        coefficients_thread(vs + lane * kPartVals, 1, sb, c, H, 0, out_thread + t * 24,
+                            out_thread + t * 24 + 4, out_thread + t * 24 + 8);
+    for (int j = 0; j < 32; j += 2) {
+        const long long ta = t0 + j, tb = t0 + j + 1;
+        // each half writes its own token's 24-float record (token index 0 in it)
+        float *rec = out_lanes + (lane < 16 ? ta : tb) * 24;
+        coefficients_16lanes(vs + j * kPartVals, vs + (j + 1) * kPartVals, 1, sb, c, H, 0, 0,
+                             ta < n && lane < 16, tb < n && lane >= 16, rec, rec + 4, rec + 8);
+    }
+}
+
+cudaError_t launch_coef_check(const float *v, const CoefArgs &c, int H, long long n,
+                              float *out_thread, float *out_lanes, cudaStream_t s) {
+    const long long blocks = (n + 31) / 32;
+    coef_check_kernel<<<static_cast<unsigned>(blocks), 32, 0, s>>>(v, c, H, n, out_thread, out_lanes);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rcp_check(uint32_t first, unsigned long long count, unsigned long long *out,
                              cudaStream_t s) {
     rcp_check_kernel<<<152 * 8, 256, 0, s>>>(first, count, out);

@@ -87,6 +87,63 @@ static __device__ __forceinline__ void coefficients_thread(const float *v, int s
     for (int i = 0; i < 4; ++i) cb[i] = make_float4(x[i][0], x[i][1], x[i][2], x[i][3]);
 }
 
+// The same coefficients formed by 16 lanes of a warp, lane l holding comb
+// entry (l / 4, l % 4): row and column sums gather their four terms by
+// shuffle and add them in the order of coefficients_thread, and every other
+// operation is the same, so the outputs are bitwise those of
+// coefficients_thread, with about a quarter of its instructions per lane
+// (the Sinkhorn steps run on the 16 entries at once): for latency, when few
+// tokens wait on it. Called by all 32 lanes of a warp: lanes 0-15 form token
+// t_lo (if valid_lo), lanes 16-31 token t_hi (if valid_hi); v_lo / v_hi as
+// in coefficients_thread.
+static __device__ __forceinline__ void coefficients_16lanes(const float *v_lo, const float *v_hi,
+                                                            int stride, const float *sb,
+                                                            const CoefArgs &c, int H, long long t_lo,
+                                                            long long t_hi, bool valid_lo,
+                                                            bool valid_hi, float *pre_out,
+                                                            float *post_out, float *comb_out) {
+    const int lane = threadIdx.x & 31;
+    const int l = lane & 15, g0 = lane & 16;          // entry, first lane of this token's group
+    const bool hi = lane >= 16;
+    const float *v = hi ? v_hi : v_lo;
+    const long long t = hi ? t_hi : t_lo;
+    const bool valid = hi ? valid_hi : valid_lo;
+    const float rstd =
+        rsqrtf(__fdiv_rn(v[24 * stride], static_cast<float>(4 * H)) + c.hc_norm_eps);
+    const float *bs = sb + 3;
+    if (l < 4) {
+        const float p = sigmoid_clamped(fmaf(v[l * stride] * rstd, sb[0], bs[l])) + c.hc_pre_eps;
+        if (valid) pre_out[t * 4 + l] = p;
+    } else if (l < 8) {
+        const float p =
+            sigmoid_clamped(fmaf(v[l * stride] * rstd, sb[1], bs[l])) * c.hc_post_mult;
+        if (valid) post_out[t * 4 + (l - 4)] = p;
+    }
+    const int r = l >> 2, k = l & 3;
+    const float eps = c.sinkhorn_eps;
+    auto at = [&](float x, int e) { return __shfl_sync(0xffffffffu, x, g0 + e); };
+    // row softmax of the logits, multiplied by the reciprocal of the row sum, plus eps
+    const float lg = fmaf(v[(8 + l) * stride] * rstd, sb[2], bs[8 + l]);
+    const float l0 = at(lg, 4 * r), l1 = at(lg, 4 * r + 1), l2 = at(lg, 4 * r + 2),
+                l3 = at(lg, 4 * r + 3);
+    const float e = expf(lg - fmaxf(fmaxf(l0, l1), fmaxf(l2, l3)));
+    const float e0 = at(e, 4 * r), e1 = at(e, 4 * r + 1), e2 = at(e, 4 * r + 2),
+                e3 = at(e, 4 * r + 3);
+    float x = fmaf(e, rcp_nr(((e0 + e1) + e2) + e3), eps);
+    auto col_normalize = [&]() {
+        const float c0 = at(x, k), c1 = at(x, 4 + k), c2 = at(x, 8 + k), c3 = at(x, 12 + k);
+        x = x * rcp_nr(((c0 + c1) + (c2 + c3)) + eps);
+    };
+    col_normalize();
+    for (int it = 1; it < c.sinkhorn_iters; ++it) {
+        const float x0 = at(x, 4 * r), x1 = at(x, 4 * r + 1), x2 = at(x, 4 * r + 2),
+                    x3 = at(x, 4 * r + 3);
+        x = x * rcp_nr((((x0 + x1) + x2) + x3) + eps);
+        col_normalize();
+    }
+    if (valid) comb_out[t * 16 + l] = x;
+}
+
 // Stages scale[0..2] and base[0..23] into sb[0..26] (threads 0..26 of the caller's group).
 static __device__ __forceinline__ void stage_coef_consts(const CoefArgs &c, float *sb, int i) {
     if (i < 3) sb[i] = __ldg(c.scale + i);

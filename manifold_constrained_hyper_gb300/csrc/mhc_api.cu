@@ -601,6 +601,29 @@ mhc_status mhc_debug_unarmed_wait(void *stream) {
         launch_unarmed_wait(dev->status, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
 }
 
+mhc_status mhc_debug_coef_check(const float *values, const float *scale, const float *base,
+                                const mhc_params *params, int hidden, int64_t tokens,
+                                float *out_thread, float *out_lanes, void *stream) {
+    if (tokens < 0) return MHC_ERR_SHAPE;
+    if (mhc_status s = check_params(params)) return s;
+    if (!hidden_ok(hidden)) return MHC_ERR_UNSUPPORTED;
+    if (tokens == 0) return MHC_OK;
+    const void *need[] = {values, scale, base, out_thread, out_lanes};
+    for (const void *p : need) {
+        if (!p) return MHC_ERR_NULL;
+        if (!aligned16(p)) return MHC_ERR_ALIGN;
+    }
+    if (tokens > 0x7FFFFFFFLL * 32) return MHC_ERR_SHAPE;
+    const size_t nv = static_cast<size_t>(tokens) * 25 * 4, no = static_cast<size_t>(tokens) * 24 * 4;
+    const Range ins[] = {{values, nv}, {scale, 12}, {base, 96}};
+    const Range outs[] = {{out_thread, no}, {out_lanes, no}};
+    if (aliasing(outs, 2, ins, 3, nullptr, nullptr)) return MHC_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    return cuda_status(launch_coef_check(values, coef_args(scale, base, params), hidden, tokens,
+                                         out_thread, out_lanes, static_cast<cudaStream_t>(stream)));
+}
+
 mhc_status mhc_debug_rcp_check(uint32_t first_bits, uint64_t count, unsigned long long *result,
                                void *stream) {
     if (!result) return MHC_ERR_NULL;

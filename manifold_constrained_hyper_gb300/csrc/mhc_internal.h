@@ -104,6 +104,8 @@ cudaError_t launch_unarmed_wait(unsigned int *status, unsigned long long timeout
 // Advances the u64 at `cell` by one (a single thread): the flag value of the
 // shifted call that follows on the stream, when that call is being captured.
 cudaError_t launch_epoch_bump(unsigned long long *cell, cudaStream_t s);
+cudaError_t launch_coef_check(const float *v, const CoefArgs &c, int H, long long n,
+                              float *out_thread, float *out_lanes, cudaStream_t s);
 cudaError_t launch_rcp_check(uint32_t first, unsigned long long count, unsigned long long *out,
                              cudaStream_t s);
 unsigned int *device_status_word();   // of the current device; NULL on failure

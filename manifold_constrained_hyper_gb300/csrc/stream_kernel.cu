@@ -654,11 +654,16 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     red[kWorkThreads + wt] = acc;
                 }
                 named_barrier_sync(kWorkBarrier, kWorkThreads);
-                if (ok && wt < nr) {
-                    const float *v = red + kWorkThreads + wt * kPartVals;
-                    coefficients_thread(v, 1, consts, a.coef, a.H,
-                                        gbase_t + static_cast<long long>(n_slices) * (r0 + wt),
-                                        a.pre_out, a.post_out, a.comb_out);
+                // 16 lanes per token (two tokens per worker warp): the end of a
+                // decode call waits on this, and one thread per token would
+                // take about twice as long
+                const int j0 = 2 * (warp - 4);
+                if (ok && j0 < nr) {
+                    const float *v = red + kWorkThreads + j0 * kPartVals;
+                    const long long t_lo = gbase_t + static_cast<long long>(n_slices) * (r0 + j0);
+                    coefficients_16lanes(v, v + kPartVals, 1, consts, a.coef, a.H, t_lo,
+                                         t_lo + n_slices, true, j0 + 1 < nr, a.pre_out, a.post_out,
+                                         a.comb_out);
                 }
                 named_barrier_sync(kWorkBarrier, kWorkThreads);
             }

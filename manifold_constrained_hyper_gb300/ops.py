@@ -27,7 +27,7 @@ EXPORTS = ("mhc_weight_bytes", "mhc_prepare_weight", "mhc_post", "mhc_workspace_
            "mhc_pre", "mhc_boundary_fused", "mhc_get_device_status", "mhc_last_timeout_site",
            "mhc_status_string", "mhc_set_wait_timeout_ns", "mhc_debug_unarmed_wait",
            "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc",
-           "mhc_debug_rcp_check", "mhc_pre_split_k")
+           "mhc_debug_rcp_check", "mhc_pre_split_k", "mhc_debug_coef_check")
 
 
 class MhcError(RuntimeError):
@@ -91,6 +91,7 @@ def load():
         "mhc_debug_unarmed_wait": (i32, [P]),
         "mhc_debug_record_between": (None, [P]),
         "mhc_debug_rcp_check": (i32, [ctypes.c_uint32, ctypes.c_uint64, P, P]),
+        "mhc_debug_coef_check": (i32, [P, P, P, PP, i32, i64, P, P, P]),
         "mhc_pre_split_k": (i32, [P, P, P, i32, P, P, P, i32, PP, i64, i32, P, P, P, P, P]),
         "mhc_plan": (i32, [i64, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     }
@@ -294,6 +295,24 @@ def mhc_set_wait_timeout_ns(ns: int):
 
 def mhc_debug_unarmed_wait(stream=None):
     _check(load().mhc_debug_unarmed_wait(_stream(stream)), "mhc_debug_unarmed_wait")
+
+
+def mhc_debug_coef_check(values, scale, base, hidden: int, params: Params | None = None,
+                         stream=None):
+    """Coefficients of the tokens of `values` [n, 25] (fp32, CUDA) formed by
+    the one-thread and the 16-lane routines: returns (out_thread, out_lanes),
+    each [n, 24] (pre 4, post 4, comb 16)."""
+    for t in (values, scale, base):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("values, scale and base must be contiguous CUDA float32 tensors")
+    n = values.shape[0]
+    p = (params or Params()).c()
+    a = torch.empty(n, 24, dtype=torch.float32, device=values.device)
+    b = torch.empty(n, 24, dtype=torch.float32, device=values.device)
+    _check(load().mhc_debug_coef_check(_p(values), _p(scale), _p(base), ctypes.byref(p),
+                                       int(hidden), n, _p(a), _p(b), _stream(stream)),
+           "mhc_debug_coef_check")
+    return a, b
 
 
 def mhc_debug_rcp_check(first_bits: int, count: int, stream=None):

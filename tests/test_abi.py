@@ -109,3 +109,17 @@ def test_argument_errors_before_any_device_work(lib):
     rest0 = list(rest)
     rest0[5] = 0
     assert lib.mhc_pre_split_k(*sk, 4, *rest0) == 0
+
+
+def test_coef_check_hook_argument_errors():
+    """The coefficient-forms hook validates before enqueuing anything (no GPU
+    needed): NULL, misaligned, negative count, aliasing outputs, T == 0."""
+    lib = ops.load()
+    p = ops.Params().c()
+    A = 0x100000
+    ok = [_P(A), _P(A * 2), _P(A * 3), ctypes.byref(p), 1024]
+    assert lib.mhc_debug_coef_check(*ok, 0, _P(A * 4), _P(A * 5), None) == 0
+    assert lib.mhc_debug_coef_check(*ok, -1, _P(A * 4), _P(A * 5), None) == 3
+    assert lib.mhc_debug_coef_check(None, *ok[1:], 8, _P(A * 4), _P(A * 5), None) == 1
+    assert lib.mhc_debug_coef_check(*ok, 8, _P(A * 4 + 8), _P(A * 5), None) == 2
+    assert lib.mhc_debug_coef_check(*ok, 8, _P(A * 4), _P(A * 4 + 16), None) == 5
