@@ -113,9 +113,32 @@ def _p(t):
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+# The current stream's raw handle without building a Stream object (the
+# public call costs several microseconds per call on some hosts).
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream=None, device=None):
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        idx = device.index if device is not None and device.index is not None \
+            else torch.cuda.current_device()
+        return _raw_stream(idx)
+    return torch.cuda.current_stream().cuda_stream
+
+
+_DEFAULT_PARAMS_C = None
+
+
+def _params_c(params):
+    """ctypes struct of `params`; the default one is built once."""
+    global _DEFAULT_PARAMS_C
+    if params is not None:
+        return params.c()
+    if _DEFAULT_PARAMS_C is None:
+        _DEFAULT_PARAMS_C = Params().c()
+    return _DEFAULT_PARAMS_C
 
 
 def _bf16(t: torch.Tensor, name: str):
@@ -193,14 +216,13 @@ def mhc_pre(residual, weight, scale, base, norm_w=None, params: Params | None = 
     """Unshifted pre: returns (layer_input, pre, post, comb)."""
     _bf16(residual, "residual")
     T, n, H = residual.shape
-    params = params or Params()
     li, pr, po, cb, ws = _outs(T, H, residual.device, layer_input, pre_out, post_out,
                                comb_out, workspace)
     nw, nwt = _nw(norm_w)
-    p = params.c()
+    p = _params_c(params)
     _check(load().mhc_pre(_p(residual), _p(weight), _p(scale), _p(base), _p(nw), nwt,
                           ctypes.byref(p), T, H, _p(li), _p(pr), _p(po), _p(cb), _p(ws),
-                          ws.numel() * ws.element_size(), _stream(stream)), "mhc_pre")
+                          ws.numel() * ws.element_size(), _stream(stream, residual.device)), "mhc_pre")
     return li, pr, po, cb
 
 
@@ -214,7 +236,6 @@ def mhc_pre_split_k(residual, dot_mix, sqrsum, scale, base, norm_w=None,
     S = dot_mix.shape[0]
     if tuple(dot_mix.shape) != (S, T, 24) or tuple(sqrsum.shape) != (S, T):
         raise ValueError("dot_mix must be [S, T, 24] and sqrsum [S, T]")
-    params = params or Params()
     dev = residual.device
     li = layer_input if layer_input is not None else torch.empty(T, H, dtype=torch.bfloat16,
                                                                  device=dev)
@@ -222,10 +243,10 @@ def mhc_pre_split_k(residual, dot_mix, sqrsum, scale, base, norm_w=None,
     po = post_out if post_out is not None else torch.empty(T, 4, device=dev)
     cb = comb_out if comb_out is not None else torch.empty(T, 4, 4, device=dev)
     nw, nwt = _nw(norm_w)
-    p = params.c()
+    p = _params_c(params)
     _check(load().mhc_pre_split_k(_p(residual), _p(dot_mix), _p(sqrsum), S, _p(scale), _p(base),
                                   _p(nw), nwt, ctypes.byref(p), T, H, _p(li), _p(pr), _p(po),
-                                  _p(cb), _stream(stream)), "mhc_pre_split_k")
+                                  _p(cb), _stream(stream, residual.device)), "mhc_pre_split_k")
     return li, pr, po, cb
 
 
@@ -238,17 +259,16 @@ def mhc_boundary_fused(x, residual, post, comb, weight, scale, base, norm_w=None
     if pre_lag is not None:
         _f32(pre_lag, "pre_lag")
     T, n, H = residual.shape
-    params = params or Params()
     if residual_out is None:
         residual_out = torch.empty_like(residual)
     li, pr, po, cb, ws = _outs(T, H, residual.device, layer_input, pre_out, post_out,
                                comb_out, workspace)
     nw, nwt = _nw(norm_w)
-    p = params.c()
+    p = _params_c(params)
     _check(load().mhc_boundary_fused(
         _p(x), _p(residual), _p(post), _p(comb), _p(pre_lag), _p(weight), _p(scale), _p(base),
         _p(nw), nwt, ctypes.byref(p), T, H, _p(residual_out), _p(li), _p(pr), _p(po), _p(cb),
-        _p(ws), ws.numel() * ws.element_size(), _stream(stream)), "mhc_boundary_fused")
+        _p(ws), ws.numel() * ws.element_size(), _stream(stream, residual.device)), "mhc_boundary_fused")
     return residual_out, li, pr, po, cb
 
 
@@ -263,7 +283,6 @@ def mhc_boundary_fused_noalloc(x, residual, post, comb, weight, scale, base, nor
     if pre_lag is not None:
         _f32(pre_lag, "pre_lag")
     T, n, H = residual.shape
-    params = params or Params()
     if residual_out is None:
         residual_out = torch.empty_like(residual)
     dev = residual.device
@@ -273,11 +292,11 @@ def mhc_boundary_fused_noalloc(x, residual, post, comb, weight, scale, base, nor
     po = post_out if post_out is not None else torch.empty(T, 4, device=dev)
     cb = comb_out if comb_out is not None else torch.empty(T, 4, 4, device=dev)
     nw, nwt = _nw(norm_w)
-    p = params.c()
+    p = _params_c(params)
     _check(load().mhc_boundary_fused_noalloc(
         _p(x), _p(residual), _p(post), _p(comb), _p(pre_lag), _p(weight), _p(scale), _p(base),
         _p(nw), nwt, ctypes.byref(p), T, H, _p(residual_out), _p(li), _p(pr), _p(po), _p(cb),
-        _stream(stream)), "mhc_boundary_fused_noalloc")
+        _stream(stream, residual.device)), "mhc_boundary_fused_noalloc")
     return residual_out, li, pr, po, cb
 
 
@@ -306,7 +325,7 @@ def mhc_debug_coef_check(values, scale, base, hidden: int, params: Params | None
         if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
             raise ValueError("values, scale and base must be contiguous CUDA float32 tensors")
     n = values.shape[0]
-    p = (params or Params()).c()
+    p = _params_c(params)
     a = torch.empty(n, 24, dtype=torch.float32, device=values.device)
     b = torch.empty(n, 24, dtype=torch.float32, device=values.device)
     _check(load().mhc_debug_coef_check(_p(values), _p(scale), _p(base), ctypes.byref(p),
