@@ -109,13 +109,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, 
           "l"(policy)
         : "memory");
 }
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, int c0, int c1, uint32_t src,
-                                             uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;"
-        ::"l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(src), "l"(policy)
-        : "memory");
-}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, int c0, int c1, int c2,
                                              uint32_t src, uint64_t policy) {
     asm volatile(
@@ -136,9 +129,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 }
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // All but the most recent bulk group have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_allbut1() {

@@ -85,7 +85,7 @@ static_assert(128 * (kRegsProducer + kRegsFinisher) + 256 * kRegsWorker <= kThre
 enum : int { SITE_PROD_READY = 1, SITE_PROD_MMA = 2, SITE_MMA_FULL = 3, SITE_MMA_READY = 4,
              SITE_WORK_FULL = 5, SITE_FIN_ACC = 6, SITE_DRAIN = 7, SITE_MMA_ACC = 8,
              SITE_FIN_SUMS = 9, SITE_WORK_SUMS = 10, SITE_TILE_FLAGS = 11, SITE_WORK_LI = 12,
-             SITE_EXIT = 13, SITE_WORK_COEF = 14 };
+             SITE_WORK_COEF = 14 };
 
 struct Coefs {
     uint64_t post2[4];       // (post[s], post[s])
