@@ -358,23 +358,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
                                                       partials_bytes(T, S) + ssql_bytes(T, S));
     sa.epoch = 0;
     sa.epoch_cell = nullptr;
-    if (mode == FUSED_SHIFTED) {
-        // Flags hold a value unique to the call. A captured call replays with
-        // its launch arguments frozen, so it takes the value from a cell that
-        // a one-thread kernel advances on every replay; other calls get it
-        // from the host.
-        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-        if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MHC_ERR_CUDA;
-        if (cap == cudaStreamCaptureStatusActive) {
-            auto *cell = reinterpret_cast<unsigned long long *>(
-                static_cast<uint8_t *>(workspace) + partials_bytes(T, S) + ssql_bytes(T, S) +
-                flags_bytes(T, S));
-            if (mhc_status s = cuda_status(launch_epoch_bump(cell, st))) return s;
-            sa.epoch_cell = cell;
-        } else {
-            sa.epoch = next_epoch();
-        }
-    }
+    sa.bump_cell = 0;
     sa.coef = coef_args(scale, base, params);
     sa.norm_w = norm_w;
     sa.nw_bf16 = norm_dtype == MHC_BF16;
@@ -399,6 +383,28 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // batch-invariant plan)
     sa.fuse_coef = mode == FUSED_SHIFTED && items <= grid && !invariant;
     sa.coef_end = mode == FUSED_SHIFTED && !sa.fuse_coef;
+    if (mode == FUSED_SHIFTED) {
+        // Flags hold a value unique to the call. A captured call replays with
+        // its launch arguments frozen, so it takes the value from a cell in
+        // the workspace: a call of one tile in a single wave advances the
+        // cell itself (its CTA 0 does, once it has seen every CTA publish, so
+        // every CTA has read the cell by then); any other captured call is
+        // preceded by a one-thread kernel that advances it. Calls outside a
+        // capture get the value from the host.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MHC_ERR_CUDA;
+        if (cap == cudaStreamCaptureStatusActive) {
+            auto *cell = reinterpret_cast<unsigned long long *>(
+                static_cast<uint8_t *>(workspace) + partials_bytes(T, S) + ssql_bytes(T, S) +
+                flags_bytes(T, S));
+            sa.epoch_cell = cell;
+            sa.bump_cell = sa.fuse_coef && tiles == 1;
+            if (!sa.bump_cell)
+                if (mhc_status s = cuda_status(launch_epoch_bump(cell, st))) return s;
+        } else {
+            sa.epoch = next_epoch();
+        }
+    }
     if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, sa, S,
                                                  static_cast<int>(items), grid, st)))
         return s;

@@ -54,7 +54,9 @@ struct StreamArgs {
     float *ssql;                 // [n_slices][T] per-slice sums of the collapse's squares
     unsigned long long *flags;   // [tiles][n_slices][4] per-call epoch flags
     unsigned long long epoch;    // this call's flag value (epoch_cell == NULL)
-    const unsigned long long *epoch_cell;   // else: read the flag value here
+    unsigned long long *epoch_cell;   // else: read the flag value here
+    int bump_cell;               // the value is the cell's plus one, and CTA 0 advances
+                                 // the cell once every CTA has published (one tile)
     CoefArgs coef;
     const void *norm_w;          // [H] or NULL
     int nw_bf16;

@@ -251,7 +251,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                   kWBytes, full(st), pol_keep);
     };
 
-    if (tid == 0) {
+    // Set-up: lane 0 of warp 1 (the MMA issuer, idle until then) fetches the
+    // tensor maps, initialises the barriers and, in a single wave, sends the
+    // first loads, while warp 0 allocates TMEM (done in series on one warp,
+    // the two took 1.2 us of a decode call).
+    if (tid == 32) {
+        tma_prefetch_desc(&tm_res);
+        if (MODE != PRE_ONLY) { tma_prefetch_desc(&tm_x); tma_prefetch_desc(&tm_rout); }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(full(i), 1);
             mbar_init(ready(i), 8);
@@ -283,10 +289,6 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     if (warp == 0) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
-    }
-    if (tid == 32) {
-        tma_prefetch_desc(&tm_res);
-        if (MODE != PRE_ONLY) { tma_prefetch_desc(&tm_x); tma_prefetch_desc(&tm_rout); }
     }
     // the finishing kernel launched after this one may start its blocks as
     // soon as SMs free up; it waits for this grid's completion itself
@@ -678,8 +680,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // this call's flag value: from the host, or (a call captured into a
         // CUDA graph) from the workspace cell the epoch kernel just advanced
         const unsigned long long epoch =
-            a.epoch_cell != nullptr ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell)
-                                    : a.epoch;
+            a.epoch_cell != nullptr
+                ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell) + (a.bump_cell ? 1 : 0)
+                : a.epoch;
         float *red = reinterpret_cast<float *>(gbase + kRedOff);
         float *rsum = red + kRsumOff;
         float *consts = red + kConstOff;
@@ -836,6 +839,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 if (a.coef_end && kn >= n_local - 2 && ok && lane == 0)
                     mbar_arrive(kn == n_local - 1 ? end_go : prev_go);
             }
+            // a captured call of one tile: every CTA has read the cell once this
+            // one has seen them all publish; advance it for the next replay
+            // (past every value this call may have used, after an abort)
+            if (a.bump_cell && blockIdx.x == 0 && q == 0 && lane == 0)
+                *reinterpret_cast<volatile unsigned long long *>(a.epoch_cell) = ok ? epoch : epoch + 1;
             if (a.fuse_coef) {
                 // warp 0's verdict, and (through the barrier) what it acquired
                 volatile int *fin_ok = reinterpret_cast<volatile int *>(gbase + kMiscOff + 32);
