@@ -293,6 +293,21 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     // the finishing kernel launched after this one may start its blocks as
     // soon as SMs free up; it waits for this grid's completion itself
     if (tid == 0) griddep_launch_dependents();
+    // the worker threads load the first item's coefficients of the previous
+    // boundary now, while the set-up runs (at the start of the item their
+    // latency delayed a decode call's first chunk by ~0.5 us)
+    float4 pv0 = make_float4(0.f, 0.f, 0.f, 0.f), lv0 = pv0;
+    float4 cv0[4] = {pv0, pv0, pv0, pv0};
+    if (MODE != PRE_ONLY && warp >= 4 && warp < 12 && n_local > 0) {
+        const long long gt0 = static_cast<long long>(item_of(0, n_slices).tile) * kTileT +
+                              (warp & 3) * 32 + lane;
+        if (gt0 < a.T) {
+            pv0 = __ldg(reinterpret_cast<const float4 *>(a.post) + gt0);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cv0[j] = __ldg(reinterpret_cast<const float4 *>(a.comb) + gt0 * 4 + j);
+            if (MODE == FUSED_SHIFTED) lv0 = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt0);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -437,9 +452,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 const long long gt = static_cast<long long>(it.tile) * kTileT + t;
                 valid = gt < a.T;
                 if (MODE != PRE_ONLY) {
-                    float4 pv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    float4 cv[4] = {pv, pv, pv, pv};
-                    if (valid) {
+                    // item 0's were loaded during the set-up
+                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 pv = k == 0 ? pv0 : z;
+                    float4 cv[4] = {k == 0 ? cv0[0] : z, k == 0 ? cv0[1] : z, k == 0 ? cv0[2] : z,
+                                    k == 0 ? cv0[3] : z};
+                    if (valid && k > 0) {
                         pv = __ldg(reinterpret_cast<const float4 *>(a.post) + gt);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
@@ -456,8 +474,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     }
                 }
                 if (MODE == FUSED_SHIFTED) {
-                    float4 lv = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (valid) lv = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt);
+                    float4 lv = k == 0 ? lv0 : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (valid && k > 0) lv = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt);
                     const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) cf.pre2[j] = f2_pack(ls[j], ls[j]);
