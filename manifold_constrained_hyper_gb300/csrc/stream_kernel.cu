@@ -46,7 +46,10 @@ namespace mhc {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kStages = 4;
+constexpr int kStages = kStreamStages;
+// Template value of the shifted form's decode variant (the decode worker
+// mapping, chosen by the host through StreamArgs::decode_map).
+constexpr int kShiftedDecode = 3;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kAccBufs = 2;                            // accumulator / sums buffers
 constexpr int kLiBufs = 3;                             // shifted: collapse buffers
@@ -71,6 +74,7 @@ constexpr int kSmemUsed = kRedOff + (kConstOff + 32) * 4;
 constexpr int kCoefGroup = 4;                          // tokens per group
 constexpr int kCoefPairs = kCoefGroup * kPartVals;     // (token, value) pairs of a group
 constexpr int kEndGroups = kWorkThreads / kCoefGroup;  // token groups per round at most
+static_assert(8 * 2 * kDecodeMaxTokens <= kAccBufs * 2 * 2 * kTileT, "decode sums in the sums area");
 static_assert(kRoundTok * kPartVals <= kFinThreads, "one combined value per thread");
 static_assert(kSmemUsed + 1024 <= 227 * 1024, "shared memory per CTA");
 constexpr int kAccCols = 64;                           // one accumulator buffer (48 used)
@@ -115,6 +119,67 @@ __device__ __forceinline__ void update8(const uint4 (&r)[4], const uint4 &xw, co
         }
         cur[s] = make_uint4(w[0], w[1], w[2], w[3]);
     }
+}
+
+// The same update for 4 hidden values (2 bf16 pairs) of every stream.
+__device__ __forceinline__ void update4(const uint2 (&r)[4], const uint2 &xw, const Coefs &c,
+                                        uint2 (&cur)[4]) {
+    const uint32_t xs[2] = {xw.x, xw.y};
+    uint32_t rs[4][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        rs[j][0] = r[j].x; rs[j][1] = r[j].y;
+    }
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        uint32_t w[2];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            uint64_t nu = mul2_ftz(c.post2[s], bf2_unpack(xs[p]));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) nu = fma2_ftz(c.comb2[j][s], bf2_unpack(rs[j][p]), nu);
+            w[p] = bf2_pack_rn(nu);
+        }
+        cur[s] = make_uint2(w[0], w[1]);
+    }
+}
+
+__device__ __forceinline__ void sq_accum2(const uint2 &v, uint64_t &acc) {
+    uint64_t a = bf2_unpack(v.x); acc = fma2(a, a, acc);
+    a = bf2_unpack(v.y); acc = fma2(a, a, acc);
+}
+
+// Lagged collapse of 4 hidden values.
+__device__ __forceinline__ uint2 collapse4(const uint2 (&cur)[4], const Coefs &c) {
+    const uint32_t cs[4][2] = {{cur[0].x, cur[0].y}, {cur[1].x, cur[1].y}, {cur[2].x, cur[2].y},
+                               {cur[3].x, cur[3].y}};
+    uint32_t w[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        uint64_t acc = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc = fma2(c.pre2[j], bf2_unpack(cs[j][p]), acc);
+        w[p] = bf2_pack_rn(acc);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+// Coefs of one token from its post, comb and lagged pre.
+__device__ __forceinline__ Coefs coefs_of(const float4 &pv, const float4 (&cv)[4], const float4 &lv) {
+    Coefs c;
+    const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+    for (int s = 0; s < 4; ++s) c.post2[s] = f2_pack(ps[s], ps[s]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float cs[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) c.comb2[j][s] = f2_pack(cs[s], cs[s]);
+    }
+    const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c.pre2[j] = f2_pack(ls[j], ls[j]);
+    return c;
 }
 
 __device__ __forceinline__ void sq_accum(const uint4 &v, uint64_t &acc) {
@@ -183,6 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_rout, const StreamArgs a, int n_slices,
               int n_items) {
+    constexpr bool kShifted = MODE == FUSED_SHIFTED || MODE == kShiftedDecode;
+    constexpr bool kDecodeMap = MODE == kShiftedDecode;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -284,7 +351,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         if (a.fuse_coef)
             for (int g = 0; g < total && g < kStages; ++g) issue_load(g);
     }
-    constexpr uint32_t kTmemCols = MODE == FUSED_SHIFTED ? 512 : kAccBufs * kAccCols;
+    constexpr uint32_t kTmemCols = kShifted && !kDecodeMap ? 512 : kAccBufs * kAccCols;
     static_assert(kAccBufs * kAccCols + kLiBufs * kLiCols <= 512, "TMEM columns");
     if (warp == 0) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -296,16 +363,17 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     // the worker threads load the first item's coefficients of the previous
     // boundary now, while the set-up runs (at the start of the item their
     // latency delayed a decode call's first chunk by ~0.5 us)
+    // (the decode mapping: token lane of the one tile)
     float4 pv0 = make_float4(0.f, 0.f, 0.f, 0.f), lv0 = pv0;
     float4 cv0[4] = {pv0, pv0, pv0, pv0};
     if (MODE != PRE_ONLY && warp >= 4 && warp < 12 && n_local > 0) {
         const long long gt0 = static_cast<long long>(item_of(0, n_slices).tile) * kTileT +
-                              (warp & 3) * 32 + lane;
+                              (kDecodeMap ? 0 : (warp & 3) * 32) + lane;
         if (gt0 < a.T) {
             pv0 = __ldg(reinterpret_cast<const float4 *>(a.post) + gt0);
 #pragma unroll
             for (int j = 0; j < 4; ++j) cv0[j] = __ldg(reinterpret_cast<const float4 *>(a.comb) + gt0 * 4 + j);
-            if (MODE == FUSED_SHIFTED) lv0 = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt0);
+            if (kShifted) lv0 = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt0);
         }
     }
     tc_fence_before();
@@ -362,7 +430,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     drain_wait(full(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
             // the stage buffers are free of this CTA's copies
-            if (MODE == FUSED_SHIFTED && a.coef_end) mbar_arrive(stages_free);
+            if (kShifted && a.coef_end) mbar_arrive(stages_free);
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
@@ -430,7 +498,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             float *sx = sums + (b * 2 + half) * 2 * kTileT;
             sx[t] = f2_lo(ssq2) + f2_hi(ssq2);
             sx[kTileT + t] = f2_lo(ssql2) + f2_hi(ssql2);
-            if (MODE == FUSED_SHIFTED) {
+            if (kShifted) {
                 tmem_st_wait();      // the item's collapse is in TMEM
                 tc_fence_before();
             }
@@ -439,7 +507,51 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         };
 
         int g = 0;
-        for (; g < total; ++g) {
+        // ---- decode mapping (one tile of at most kDecodeMaxTokens tokens, one
+        // item of at most kStages chunks, so no stage is refilled): the
+        // elementwise work of a chunk is instruction-bound per warp, and with
+        // the usual mapping only the warps of the first token quarter or two
+        // have tokens. Here worker warp w' = warp - 4 takes hidden unit
+        // w' / 2, pairs 2 (w' % 2) and 2 (w' % 2) + 1, of token lane of every
+        // chunk (a quarter of the usual work per thread). The collapse goes
+        // into the chunk's x tile (consumed by
+        // then, and read by neither the copy out nor the MMA) instead of TMEM,
+        // whose lane quarters belong to fixed warps; the finishers read it
+        // there. The per-token sums of squares are handed over per warp.
+        constexpr bool dmap = kDecodeMap;
+        if (dmap && total > 0) {
+            const int wq = warp - 4, un = wq >> 1, pq = wq & 1;
+            const Coefs cd = coefs_of(pv0, cv0, lv0);
+            uint64_t sq = 0, sql = 0;
+            for (; g < total; ++g) {
+                const uint32_t sb = base + g * kStageBytes;
+                if (!mbar_wait(full(g), 0, abort_flag, tmo, a.status, SITE_WORK_FULL)) break;
+                if (lane < a.T) {
+                    const uint32_t off = lane * kRowBytes + 16u * (un ^ ((lane >> 1) & 3)) + 8u * pq;
+                    uint2 r[4], cur[4];
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2) r[s2] = ld_shared_v2(sb + s2 * kTileT * kRowBytes + off);
+                    update4(r, ld_shared_v2(sb + kResBytes + off), cd, cur);
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2) {
+                        st_shared_v2(sb + s2 * kTileT * kRowBytes + off, cur[s2]);
+                        sq_accum2(cur[s2], sq);
+                    }
+                    const uint2 li = collapse4(cur, cd);
+                    st_shared_v2(sb + kResBytes + off, li);
+                    sq_accum2(li, sql);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ready(g));
+            }
+            // sums of warp w' for token lane at [w'][0 / 1][lane] of the item's sums buffer
+            sums[(wq * 2 + 0) * kDecodeMaxTokens + lane] = f2_lo(sq) + f2_hi(sq);
+            sums[(wq * 2 + 1) * kDecodeMaxTokens + lane] = f2_lo(sql) + f2_hi(sql);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sums_full(0));
+        }
+        for (; !dmap && g < total; ++g) {
             const int st = g % kStages;
             const uint32_t ph = (g / kStages) & 1;
             const int k = g / d, c = g % d;
@@ -473,7 +585,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                         for (int s = 0; s < 4; ++s) cf.comb2[j][s] = f2_pack(cs[s], cs[s]);
                     }
                 }
-                if (MODE == FUSED_SHIFTED) {
+                if (kShifted) {
                     float4 lv = k == 0 ? lv0 : make_float4(0.f, 0.f, 0.f, 0.f);
                     if (valid && k > 0) lv = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt);
                     const float ls[4] = {lv.x, lv.y, lv.z, lv.w};
@@ -512,21 +624,21 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             st_shared_v4(sb + s * kTileT * kRowBytes + off, cur[s]);
                             sq_accum(cur[s], ssq2);
                         }
-                        if (MODE == FUSED_SHIFTED) {
+                        if (kShifted) {
                             li = collapse8(cur, cf);
                             sq_accum(li, ssql2);
                         }
                     }
                 }
                 // this thread's 8 collapse values of the unit, kept in TMEM
-                if (MODE == FUSED_SHIFTED) tmem_st4(li_chunk + 4 * uu, li);
+                if (kShifted) tmem_st4(li_chunk + 4 * uu, li);
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(ready(st));
         }
         // the last item (after an abort the finishers only get their barriers)
-        if (total > 0) hand_over(g < total ? g / d : n_local - 1);
+        if (!dmap && total > 0) hand_over(g < total ? g / d : n_local - 1);
 
         // ---- several items per CTA: the coefficients of every token of the
         // CTA's items, formed by the workers once they have streamed their
@@ -544,7 +656,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // sum in place; then a thread per token forms pre / post / comb.
         // Worker thread 0 lays out each round in shared memory, so every
         // worker warp takes part in each barrier, also after an abort.
-        if (MODE == FUSED_SHIFTED && a.coef_end) {
+        if (kShifted && a.coef_end) {
             const int wt = tid - 4 * 32;                   // 0..255 among the workers
             bool ok = g == total && mbar_wait(stages_free, 0, abort_flag, tmo, a.status, SITE_WORK_COEF);
             ok = __all_sync(0xffffffffu, ok);
@@ -722,10 +834,21 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 bool ok = mbar_wait(sums_full(b), ph, abort_flag, tmo, a.status, SITE_FIN_SUMS);
                 ok = mbar_wait(acc_full(b), ph, abort_flag, tmo, a.status, SITE_FIN_ACC) && ok;
                 tc_fence_after();
-                const float *s0 = sums + (b * 2 + 0) * 2 * kTileT;
-                const float *s1 = sums + (b * 2 + 1) * 2 * kTileT;
-                const float ssq = s0[t] + s1[t];
-                const float ssql = s0[kTileT + t] + s1[kTileT + t];
+                float ssq = 0.f, ssql = 0.f;
+                if (kDecodeMap) {
+                    // the eight worker warps' sums, in warp order
+                    if (t < kDecodeMaxTokens) {
+                        for (int w2 = 0; w2 < 8; ++w2) {
+                            ssq += sums[(w2 * 2 + 0) * kDecodeMaxTokens + t];
+                            ssql += sums[(w2 * 2 + 1) * kDecodeMaxTokens + t];
+                        }
+                    }
+                } else {
+                    const float *s0 = sums + (b * 2 + 0) * 2 * kTileT;
+                    const float *s1 = sums + (b * 2 + 1) * 2 * kTileT;
+                    ssq = s0[t] + s1[t];
+                    ssql = s0[kTileT + t] + s1[kTileT + t];
+                }
                 uint32_t v[48];
                 const uint32_t acc = tmem_base + b * kAccCols + lane_off;
                 tmem_ld16(acc + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
@@ -754,7 +877,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
 #pragma unroll
                         for (int i = 0; i < kTokStride / 4; ++i)
                             dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                    } else if (MODE == FUSED_SHIFTED) {
+                    } else if (kShifted) {
                         // the token's 128-byte record of this slice: four 32-byte
                         // stores of whole sectors, kept in L2 for the end of the
                         // kernel (where a token group's records of every slice
@@ -781,13 +904,13 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                                           __uint_as_float(v[i]) + __uint_as_float(v[24 + i]), pol_keep);
                         st_global_f32(dst + 24 * kTileT, ssq, pol_keep);
                     }
-                    if (MODE == FUSED_SHIFTED)
+                    if (kShifted)
                         a.ssql[static_cast<size_t>(it.slice) * a.T + gt] = ssql;
                 }
                 // publish this quarter of the item to the tile's other slices
                 // (a single wave: the whole item at once, after the four
                 // finisher warps have written, with one flag)
-                if (MODE == FUSED_SHIFTED) {
+                if (kShifted) {
                     unsigned long long *flag =
                         a.flags + (static_cast<long long>(it.tile) * n_slices + it.slice) * 4;
                     if (a.fuse_coef) {
@@ -799,7 +922,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     }
                 }
             }
-            if (MODE != FUSED_SHIFTED || k == 0) continue;
+            if (!kShifted || k == 0) continue;
 
             // ---- layer input of item kn = k - 1
             const int kn = k - 1, lb = kn % kLiBufs;
@@ -938,8 +1061,20 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 const float w_cur = w_next;
                 if (c + 1 < d) w_next = nw_lane(c + 1);
                 uint32_t w16[16];
-                tmem_ld16(li + c * 16, w16);
-                tmem_ld_wait();
+                if (kDecodeMap) {
+                    // the collapse of chunk c sits in its stage's x tile, row t
+                    const uint32_t row = base + c * kStageBytes + kResBytes + (t & (kTileT - 1)) * kRowBytes;
+                    const uint32_t swt = (t >> 1) & 3;
+#pragma unroll
+                    for (int u2 = 0; u2 < 4; ++u2) {
+                        const uint4 q4 = ld_shared_v4(row + 16u * (u2 ^ swt));
+                        w16[4 * u2] = q4.x; w16[4 * u2 + 1] = q4.y;
+                        w16[4 * u2 + 2] = q4.z; w16[4 * u2 + 3] = q4.w;
+                    }
+                } else {
+                    tmem_ld16(li + c * 16, w16);
+                    tmem_ld_wait();
+                }
                 const long long h0 = chunk_hidden(it.slice, c, n_slices);
                 uint16_t *dst = a.layer_input + gt * a.H + h0;
 #pragma unroll
@@ -999,7 +1134,7 @@ cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtenso
         if (e != cudaSuccess) return e;
         opted.fetch_or(bit, std::memory_order_release);
     }
-    if (MODE != FUSED_SHIFTED) {
+    if (MODE != FUSED_SHIFTED && MODE != kShiftedDecode) {
         kern<<<grid, kThreads, smem, s>>>(res, x, rout, a, n_slices, n_items);
         return cudaGetLastError();
     }
@@ -1029,7 +1164,8 @@ cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x
         case FUSED_UNSHIFTED:
             return launch_t<FUSED_UNSHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
         case FUSED_SHIFTED:
-            return launch_t<FUSED_SHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
+            return a.decode_map ? launch_t<kShiftedDecode>(res, x, rout, a, n_slices, n_items, grid, s)
+                                : launch_t<FUSED_SHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
