@@ -383,7 +383,9 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // batch-invariant plan)
     sa.fuse_coef = mode == FUSED_SHIFTED && items <= grid && !invariant;
     sa.coef_end = mode == FUSED_SHIFTED && !sa.fuse_coef;
-    sa.decode_map = sa.fuse_coef && T <= kDecodeMaxTokens && w / kChunk <= kStreamStages;
+    sa.decode_map = sa.fuse_coef && T <= kDecodeMaxTokens && w / kChunk <= kStreamStages
+                        ? (T <= 32 ? 1 : 2)
+                        : 0;
     if (mode == FUSED_SHIFTED) {
         // Flags hold a value unique to the call. A captured call replays with
         // its launch arguments frozen, so it takes the value from a cell in

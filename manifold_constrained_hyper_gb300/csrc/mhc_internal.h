@@ -67,9 +67,10 @@ struct StreamArgs {
     int coef_end;                // shifted, several items per CTA: the workers form
                                  // them after the CTA's last item (record layout)
     int decode_map;              // shifted, one tile of at most kDecodeMaxTokens tokens in
-                                 // a single wave, at most kStreamStages chunks: every worker
-                                 // warp takes a quarter unit of each chunk, the collapse
-                                 // stays in the stage's x tile (see the streaming kernel)
+                                 // a single wave, at most kStreamStages chunks: the decode
+                                 // mapping of the worker warps, 1 up to 32 tokens, 2 above,
+                                 // the collapse kept in the stage's x tile (see the
+                                 // streaming kernel); 0 otherwise
     int box_rows;                // one tile: token rows per residual / x box (the
                                  // residual maps then hold one stream per box); 0: 128
 };
@@ -89,7 +90,7 @@ struct FinishArgs {
 
 constexpr int kGridCap = 152;                       // persistent CTAs: one per GB300 SM
 constexpr int kStreamStages = 4;                    // pipeline stages of the streaming kernel
-constexpr int kDecodeMaxTokens = 32;                // most tokens of the decode worker mapping
+constexpr int kDecodeMaxTokens = 64;                // most tokens of the decode worker mapping
 constexpr int kMaxSplits = 64;                      // split-K pre: most K splits accepted
 
 size_t stream_smem_bytes();

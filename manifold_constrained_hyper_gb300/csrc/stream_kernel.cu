@@ -47,9 +47,11 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kStages = kStreamStages;
-// Template value of the shifted form's decode variant (the decode worker
-// mapping, chosen by the host through StreamArgs::decode_map).
+// Template values of the shifted form's decode variants (the decode worker
+// mapping, chosen by the host through StreamArgs::decode_map): up to 32
+// tokens (quarter units) and 33 to kDecodeMaxTokens tokens (whole units).
 constexpr int kShiftedDecode = 3;
+constexpr int kShiftedDecodeHalf = 4;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kAccBufs = 2;                            // accumulator / sums buffers
 constexpr int kLiBufs = 3;                             // shifted: collapse buffers
@@ -248,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_rout, const StreamArgs a, int n_slices,
               int n_items) {
-    constexpr bool kShifted = MODE == FUSED_SHIFTED || MODE == kShiftedDecode;
-    constexpr bool kDecodeMap = MODE == kShiftedDecode;
+    constexpr bool kDecodeMap = MODE == kShiftedDecode || MODE == kShiftedDecodeHalf;
+    constexpr bool kShifted = MODE == FUSED_SHIFTED || kDecodeMap;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -368,7 +370,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     float4 cv0[4] = {pv0, pv0, pv0, pv0};
     if (MODE != PRE_ONLY && warp >= 4 && warp < 12 && n_local > 0) {
         const long long gt0 = static_cast<long long>(item_of(0, n_slices).tile) * kTileT +
-                              (kDecodeMap ? 0 : (warp & 3) * 32) + lane;
+                              (kDecodeMap ? (MODE == kShiftedDecodeHalf ? ((warp - 4) & 1) * 32 : 0)
+                                          : (warp & 3) * 32) + lane;
         if (gt0 < a.T) {
             pv0 = __ldg(reinterpret_cast<const float4 *>(a.post) + gt0);
 #pragma unroll
@@ -511,43 +514,67 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // item of at most kStages chunks, so no stage is refilled): the
         // elementwise work of a chunk is instruction-bound per warp, and with
         // the usual mapping only the warps of the first token quarter or two
-        // have tokens. Here worker warp w' = warp - 4 takes hidden unit
-        // w' / 2, pairs 2 (w' % 2) and 2 (w' % 2) + 1, of token lane of every
-        // chunk (a quarter of the usual work per thread). The collapse goes
+        // have tokens. Here worker warp w' = warp - 4 takes hidden unit w' / 2
+        // of every chunk: of token lane, pairs 2 (w' % 2) and 2 (w' % 2) + 1
+        // (up to 32 tokens: a quarter of the usual work per thread), or whole
+        // for token lane + 32 (w' % 2) (33 to 64 tokens: half). The collapse goes
         // into the chunk's x tile (consumed by
         // then, and read by neither the copy out nor the MMA) instead of TMEM,
         // whose lane quarters belong to fixed warps; the finishers read it
         // there. The per-token sums of squares are handed over per warp.
         constexpr bool dmap = kDecodeMap;
         if (dmap && total > 0) {
+            // up to 32 tokens: warp w' takes unit w' / 2, pair-half w' % 2, of
+            // token lane; 33 to 64: unit w' / 2 whole, of token lane + 32 (w' % 2)
+            constexpr bool quarter = MODE == kShiftedDecode;
             const int wq = warp - 4, un = wq >> 1, pq = wq & 1;
-            const Coefs cd = coefs_of(pv0, cv0, lv0);
+            const int tt = quarter ? lane : lane + 32 * pq;
+            const Coefs cd = coefs_of(pv0, cv0, lv0);      // token tt's, loaded in the set-up
             uint64_t sq = 0, sql = 0;
             for (; g < total; ++g) {
                 const uint32_t sb = base + g * kStageBytes;
                 if (!mbar_wait(full(g), 0, abort_flag, tmo, a.status, SITE_WORK_FULL)) break;
-                if (lane < a.T) {
-                    const uint32_t off = lane * kRowBytes + 16u * (un ^ ((lane >> 1) & 3)) + 8u * pq;
-                    uint2 r[4], cur[4];
+                if (tt < a.T) {
+                    const uint32_t unit = tt * kRowBytes + 16u * (un ^ ((tt >> 1) & 3));
+                    if (quarter) {
+                        const uint32_t off = unit + 8u * pq;
+                        uint2 r[4], cur[4];
 #pragma unroll
-                    for (int s2 = 0; s2 < 4; ++s2) r[s2] = ld_shared_v2(sb + s2 * kTileT * kRowBytes + off);
-                    update4(r, ld_shared_v2(sb + kResBytes + off), cd, cur);
+                        for (int s2 = 0; s2 < 4; ++s2) r[s2] = ld_shared_v2(sb + s2 * kTileT * kRowBytes + off);
+                        update4(r, ld_shared_v2(sb + kResBytes + off), cd, cur);
 #pragma unroll
-                    for (int s2 = 0; s2 < 4; ++s2) {
-                        st_shared_v2(sb + s2 * kTileT * kRowBytes + off, cur[s2]);
-                        sq_accum2(cur[s2], sq);
+                        for (int s2 = 0; s2 < 4; ++s2) {
+                            st_shared_v2(sb + s2 * kTileT * kRowBytes + off, cur[s2]);
+                            sq_accum2(cur[s2], sq);
+                        }
+                        const uint2 li = collapse4(cur, cd);
+                        st_shared_v2(sb + kResBytes + off, li);
+                        sq_accum2(li, sql);
+                    } else {
+                        uint4 r[4], cur[4];
+#pragma unroll
+                        for (int s2 = 0; s2 < 4; ++s2) r[s2] = ld_shared_v4(sb + s2 * kTileT * kRowBytes + unit);
+                        update8(r, ld_shared_v4(sb + kResBytes + unit), cd, cur);
+#pragma unroll
+                        for (int s2 = 0; s2 < 4; ++s2) {
+                            st_shared_v4(sb + s2 * kTileT * kRowBytes + unit, cur[s2]);
+                            sq_accum(cur[s2], sq);
+                        }
+                        const uint4 li = collapse8(cur, cd);
+                        st_shared_v4(sb + kResBytes + unit, li);
+                        sq_accum(li, sql);
                     }
-                    const uint2 li = collapse4(cur, cd);
-                    st_shared_v2(sb + kResBytes + off, li);
-                    sq_accum2(li, sql);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ready(g));
             }
-            // sums of warp w' for token lane at [w'][0 / 1][lane] of the item's sums buffer
-            sums[(wq * 2 + 0) * kDecodeMaxTokens + lane] = f2_lo(sq) + f2_hi(sq);
-            sums[(wq * 2 + 1) * kDecodeMaxTokens + lane] = f2_lo(sql) + f2_hi(sql);
+            // sums of warp w' for token t at [w'][0 / 1][t] of the item's sums
+            // buffer; a warp that has no share of token t leaves zeros there
+            sums[(wq * 2 + 0) * kDecodeMaxTokens + tt] = f2_lo(sq) + f2_hi(sq);
+            sums[(wq * 2 + 1) * kDecodeMaxTokens + tt] = f2_lo(sql) + f2_hi(sql);
+            sums[(wq * 2 + 0) * kDecodeMaxTokens + (tt ^ 32)] = 0.f;
+            sums[(wq * 2 + 1) * kDecodeMaxTokens + (tt ^ 32)] = 0.f;
             __syncwarp();
             if (lane == 0) mbar_arrive(sums_full(0));
         }
@@ -1134,7 +1161,7 @@ cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtenso
         if (e != cudaSuccess) return e;
         opted.fetch_or(bit, std::memory_order_release);
     }
-    if (MODE != FUSED_SHIFTED && MODE != kShiftedDecode) {
+    if (MODE != FUSED_SHIFTED && MODE != kShiftedDecode && MODE != kShiftedDecodeHalf) {
         kern<<<grid, kThreads, smem, s>>>(res, x, rout, a, n_slices, n_items);
         return cudaGetLastError();
     }
@@ -1164,8 +1191,11 @@ cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x
         case FUSED_UNSHIFTED:
             return launch_t<FUSED_UNSHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
         case FUSED_SHIFTED:
-            return a.decode_map ? launch_t<kShiftedDecode>(res, x, rout, a, n_slices, n_items, grid, s)
-                                : launch_t<FUSED_SHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
+            if (a.decode_map == 1)
+                return launch_t<kShiftedDecode>(res, x, rout, a, n_slices, n_items, grid, s);
+            if (a.decode_map == 2)
+                return launch_t<kShiftedDecodeHalf>(res, x, rout, a, n_slices, n_items, grid, s);
+            return launch_t<FUSED_SHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
         default: return cudaErrorInvalidValue;
     }
 }
