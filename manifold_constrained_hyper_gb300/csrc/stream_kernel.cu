@@ -60,7 +60,8 @@ constexpr int kBarBytes = 256;
 constexpr int kSumsOff = kBarOff + kBarBytes;          // [buffers][2 halves][2 sums][128] fp32
 constexpr int kMiscOff = kSumsOff + kAccBufs * 2 * 2 * kTileT * 4;
 // scratch: the workers' coefficient reduction [256] + [128], the finishers'
-// collapse sums [128], the coefficient constants [32] (fp32)
+// collapse sums [128], the coefficient constants [32], each finisher warp's
+// copy of its item's layer norm weights [4][8 chunks][32] (fp32)
 constexpr int kRedOff = kMiscOff + 64;
 constexpr int kWorkThreads = 256;
 constexpr int kFinThreads = 128;
@@ -69,7 +70,8 @@ constexpr int kFinBarrier = 1;                         // named barrier of the f
 constexpr int kWorkBarrier = 2;                        // named barrier of the worker warps
 constexpr int kRsumOff = kWorkThreads + kFinThreads;   // float offsets within the scratch
 constexpr int kConstOff = kRsumOff + kFinThreads;
-constexpr int kSmemUsed = kRedOff + (kConstOff + 32) * 4;
+constexpr int kNwOff = kConstOff + 32;
+constexpr int kSmemUsed = kRedOff + (kNwOff + 4 * 8 * 32) * 4;
 // shifted, several items per CTA: the coefficients are formed after the
 // CTA's last item, from token groups' partial records [4][S][32] fp32 landed
 // by bulk copies in the (then free) stage buffers
@@ -956,6 +958,31 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             const Item it = item_of(kn, n_slices);
             const long long gt = static_cast<long long>(it.tile) * kTileT + t;
             bool ok = __all_sync(0xffffffffu, !*abort_flag);
+            // 32 hidden per chunk; lane l fetches norm weight l of the chunk
+            // (one coalesced load per warp) and the values go round by shuffle
+            auto nw_lane = [&](int c) -> float {
+                if (a.norm_w == nullptr) return 0.f;
+                const long long h = chunk_hidden(it.slice, c, n_slices) + lane;
+                if (a.nw_bf16)
+                    return __uint_as_float(static_cast<uint32_t>(
+                                               __ldg(static_cast<const uint16_t *>(a.norm_w) + h))
+                                           << 16);
+                return __ldg(static_cast<const float *>(a.norm_w) + h);
+            };
+            // every chunk's weights (at most 8 chunks) are fetched before the
+            // wait for the tile, off the end of a decode call's critical path,
+            // and parked in this warp's shared copy (each lane reads back the
+            // values it wrote), so that no registers are held across the
+            // sums of squares below
+            float *nws = red + kNwOff + q * (8 * kChunk);
+            {
+                float nwv[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) nwv[c] = c < d ? nw_lane(c) : 0.f;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    if (c < d) nws[c * kChunk + lane] = nwv[c];
+            }
             // every slice of the tile published. The layer RMSNorm needs the
             // flags of this warp's token quarter only: one acquire read per
             // slice, spread over the lanes. Forming the coefficients here
@@ -1071,22 +1098,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 }
                 rstd_li = rsqrtf(__fdiv_rn(sl, static_cast<float>(a.H)) + a.coef.norm_eps);
             }
-            // 32 hidden per chunk; lane l fetches norm weight l of the chunk
-            // (one coalesced load per warp) and the values go round by shuffle
-            auto nw_lane = [&](int c) -> float {
-                if (a.norm_w == nullptr) return 0.f;
-                const long long h = chunk_hidden(it.slice, c, n_slices) + lane;
-                if (a.nw_bf16)
-                    return __uint_as_float(static_cast<uint32_t>(
-                                               __ldg(static_cast<const uint16_t *>(a.norm_w) + h))
-                                           << 16);
-                return __ldg(static_cast<const float *>(a.norm_w) + h);
-            };
             const uint32_t li = tmem_base + lane_off + kLiCol + lb * kLiCols;
-            float w_next = nw_lane(0);
             for (int c = 0; c < d; ++c) {
-                const float w_cur = w_next;
-                if (c + 1 < d) w_next = nw_lane(c + 1);
+                const float w_cur = nws[c * kChunk + lane];
                 uint32_t w16[16];
                 if (kDecodeMap) {
                     // the collapse of chunk c sits in its stage's x tile, row t
