@@ -127,9 +127,10 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *residual, const float *po
  * at (T, H): per-token partial mixes and sums of squares of every hidden
  * slice, and the shifted form's publication flags. 0 when T == 0. It needs
  * no initialisation. Calls may be captured into a CUDA graph (they allocate
- * nothing and never synchronise): a captured shifted call enqueues one extra
- * one-thread kernel that gives each replay its own flag value, so replays
- * may run with new contents in the same buffers. Calls that share a
+ * nothing and never synchronise): a captured shifted call takes its flag
+ * value from a cell in the workspace and advances the cell itself, so each
+ * replay has its own value and replays may run with new contents in the
+ * same buffers (still one kernel per call). Calls that share a
  * workspace must not overlap in time. */
 size_t mhc_workspace_bytes(int64_t tokens, int hidden);
 

@@ -333,9 +333,6 @@ __global__ void __launch_bounds__(kColThreads) collapse_unshifted_kernel(const F
             norm8(li_s[u], rstd_li, a.norm_w, a.nw_bf16, 8LL * u);
 }
 
-// ------------------------------------------------------------ epoch cell
-__global__ void epoch_bump_kernel(unsigned long long *cell) { *cell = *cell + 1; }
-
 // ------------------------------------------------------------ reciprocal check
 // Counts the bit patterns in [first, first + count) whose rcp_nr differs from
 // the correctly rounded reciprocal; out[0] += count, out[1] = min(pattern).
@@ -464,11 +461,6 @@ cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s) {
     if (cudaError_t e = ensure_dynamic_smem(collapse_unshifted_kernel, g_optin_collapse, smem))
         return e;
     collapse_unshifted_kernel<<<static_cast<unsigned>(a.T), kColThreads, smem, s>>>(a);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_epoch_bump(unsigned long long *cell, cudaStream_t s) {
-    epoch_bump_kernel<<<1, 1, 0, s>>>(cell);
     return cudaGetLastError();
 }
 

@@ -359,6 +359,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.epoch = 0;
     sa.epoch_cell = nullptr;
     sa.bump_cell = 0;
+    sa.bump_poll = 0;
     sa.coef = coef_args(scale, base, params);
     sa.norm_w = norm_w;
     sa.nw_bf16 = norm_dtype == MHC_BF16;
@@ -389,11 +390,11 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     if (mode == FUSED_SHIFTED) {
         // Flags hold a value unique to the call. A captured call replays with
         // its launch arguments frozen, so it takes the value from a cell in
-        // the workspace: a call of one tile in a single wave advances the
-        // cell itself (its CTA 0 does, once it has seen every CTA publish, so
-        // every CTA has read the cell by then); any other captured call is
-        // preceded by a one-thread kernel that advances it. Calls outside a
-        // capture get the value from the host.
+        // the workspace (plus one) and advances the cell itself once every
+        // CTA has read it: CTA 0 does, after it has seen every CTA publish
+        // (a call of one tile in a single wave, whose CTA 0 waits for them
+        // all anyway) or every CTA's first item publish (any other call).
+        // Calls outside a capture get the value from the host.
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MHC_ERR_CUDA;
         if (cap == cudaStreamCaptureStatusActive) {
@@ -402,8 +403,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
                 flags_bytes(T, S));
             sa.epoch_cell = cell;
             sa.bump_cell = sa.fuse_coef && tiles == 1;
-            if (!sa.bump_cell)
-                if (mhc_status s = cuda_status(launch_epoch_bump(cell, st))) return s;
+            sa.bump_poll = !sa.bump_cell;
         } else {
             sa.epoch = next_epoch();
         }

@@ -54,9 +54,12 @@ struct StreamArgs {
     float *ssql;                 // [n_slices][T] per-slice sums of the collapse's squares
     unsigned long long *flags;   // [tiles][n_slices][4] per-call epoch flags
     unsigned long long epoch;    // this call's flag value (epoch_cell == NULL)
-    unsigned long long *epoch_cell;   // else: read the flag value here
-    int bump_cell;               // the value is the cell's plus one, and CTA 0 advances
-                                 // the cell once every CTA has published (one tile)
+    unsigned long long *epoch_cell;   // else: the flag value is the cell's plus one,
+                                      // and the call advances the cell itself:
+    int bump_cell;               // one tile: CTA 0's finishers, once they have seen
+                                 // every CTA publish
+    int bump_poll;               // several tiles: warp 2 of CTA 0, once every CTA's
+                                 // first item has published
     CoefArgs coef;
     const void *norm_w;          // [H] or NULL
     int nw_bf16;
@@ -112,7 +115,6 @@ cudaError_t launch_unarmed_wait(unsigned int *status, unsigned long long timeout
                                 cudaStream_t s);
 // Advances the u64 at `cell` by one (a single thread): the flag value of the
 // shifted call that follows on the stream, when that call is being captured.
-cudaError_t launch_epoch_bump(unsigned long long *cell, cudaStream_t s);
 cudaError_t launch_coef_check(const float *v, const CoefArgs &c, int H, long long n,
                               float *out_thread, float *out_lanes, cudaStream_t s);
 cudaError_t launch_rcp_check(uint32_t first, unsigned long long count, unsigned long long *out,

@@ -93,7 +93,7 @@ static_assert(128 * (kRegsProducer + kRegsFinisher) + 256 * kRegsWorker <= kThre
 enum : int { SITE_PROD_READY = 1, SITE_PROD_MMA = 2, SITE_MMA_FULL = 3, SITE_MMA_READY = 4,
              SITE_WORK_FULL = 5, SITE_FIN_ACC = 6, SITE_DRAIN = 7, SITE_MMA_ACC = 8,
              SITE_FIN_SUMS = 9, SITE_WORK_SUMS = 10, SITE_TILE_FLAGS = 11, SITE_WORK_LI = 12,
-             SITE_WORK_COEF = 14 };
+             SITE_WORK_COEF = 14, SITE_EPOCH = 15 };
 
 struct Coefs {
     uint64_t post2[4];       // (post[s], post[s])
@@ -474,6 +474,43 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 drain_wait(mma_done(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
         }
+        if (warp == 2 && a.bump_poll && blockIdx.x == 0) {
+            // ------------------------------------------------ epoch advance
+            // A captured call of several tiles. CTA b's first item is item b,
+            // and the flag of its first token quarter (word 4b) is written by
+            // the thread that read the cell, with the value derived from it:
+            // once every CTA's is seen, no CTA of this call reads the cell
+            // again, and it is advanced for the next replay.
+            const unsigned long long e =
+                *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell) + 1;
+            const int nb = static_cast<int>(gridDim.x);
+            bool done = false;
+            uint64_t t_start = 0;
+            for (;;) {
+                unsigned long long v[kGridCap / 32 + 1];
+#pragma unroll
+                for (int i = 0; i <= kGridCap / 32; ++i)
+                    v[i] = lane + 32 * i < nb ? flag_relaxed(a.flags + 4LL * (lane + 32 * i)) : e;
+                bool seen = true;
+#pragma unroll
+                for (int i = 0; i <= kGridCap / 32; ++i) seen = seen && v[i] == e;
+                if (__all_sync(0xffffffffu, seen)) {
+                    done = true;
+                    break;
+                }
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+                const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+                if (t_start == 0) {
+                    t_start = now;
+                } else if (now - t_start > tmo) {
+                    if (lane == 0) record_failure(a.status, 7, SITE_EPOCH);
+                    break;
+                }
+                nanosleep_ns(1000);
+            }
+            // after a failure: past every value this call may have used
+            if (lane == 0) *reinterpret_cast<volatile unsigned long long *>(a.epoch_cell) = done ? e : e + 1;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(exit_bar);
         if (warp == 0) {
@@ -837,16 +874,22 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         regs_dec_finisher();
         const int q = warp & 3;
         // this call's flag value: from the host, or (a call captured into a
-        // CUDA graph) from the workspace cell the epoch kernel just advanced
-        const unsigned long long epoch =
-            a.epoch_cell != nullptr
-                ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell) + (a.bump_cell ? 1 : 0)
-                : a.epoch;
+        // CUDA graph) one more than the workspace cell's, which the call then
+        // advances itself. One thread reads the cell and hands the value to
+        // the other finishers, so the first flag this CTA publishes (written
+        // by that thread) shows that the CTA is done with the cell.
+        volatile unsigned long long *epoch_sh =
+            reinterpret_cast<volatile unsigned long long *>(gbase + kMiscOff + 48);
+        if (tid == 12 * 32)
+            *epoch_sh = a.epoch_cell != nullptr
+                            ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell) + 1
+                            : a.epoch;
         float *red = reinterpret_cast<float *>(gbase + kRedOff);
         float *rsum = red + kRsumOff;
         float *consts = red + kConstOff;
         stage_coef_consts(a.coef, consts, tid - 12 * 32);
         named_barrier_sync(kFinBarrier, kFinThreads);
+        const unsigned long long epoch = *epoch_sh;
         const int t = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint64_t pol_out = policy_evict_first();

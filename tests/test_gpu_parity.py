@@ -378,6 +378,68 @@ def test_calls_capture_into_a_cuda_graph_and_replay_with_new_inputs(T, H):
             assert torch.equal(v, got), (form, k)
 
 
+@pytest.mark.parametrize("T,H", [(64, 7168), (512, 7168), (2048, 7168)])
+def test_captured_chain_of_shifted_calls_sharing_a_workspace(T, H):
+    """Three shifted calls captured back to back into one graph share one
+    workspace, each reading the residual the one before it wrote. Each call
+    needs a flag value of its own: one that took the previous call's would
+    find every flag already set and read that call's partials, formed from
+    another residual. Replayed twice, the chain gives the eager chain's
+    results bit for bit. Plans: one tile, several tiles in a single wave,
+    several items per CTA."""
+    dev = "cuda"
+    n = 3
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    A = synth.make_inputs(T, H, seed=720 + T)
+    res0, x = bf(A["residual"]), bf(A["x"])
+    post, comb, pl = f32(A["post"]), f32(A["comb"]), f32(A["pre_lag"])
+    scale, base, nw = f32(A["scale"]), f32(A["base"]), f32(A["norm_w"])
+    w = ops.mhc_prepare_weight(f32(A["fn"]))
+    ws = torch.empty(ops.workspace_bytes(T, H), dtype=torch.uint8, device=dev)
+
+    def new_outs():
+        return [dict(residual_out=torch.empty_like(res0),
+                     layer_input=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                     pre_out=torch.empty(T, 4, device=dev), post_out=torch.empty(T, 4, device=dev),
+                     comb_out=torch.empty(T, 4, 4, device=dev)) for _ in range(n)]
+
+    def chain(outs, stream=None):
+        r = res0
+        for o in outs:
+            ops.mhc_boundary_fused(x, r, post, comb, w, scale, base, nw, pl, workspace=ws,
+                                   stream=stream, **o)
+            r = o["residual_out"]
+
+    eager = new_outs()
+    chain(eager)
+    torch.cuda.synchronize()
+    cap = new_outs()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        chain(cap, stream=s)                     # warm-up on the capture stream
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            chain(cap, stream=s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for o in cap:
+            for v in o.values():
+                v.zero_()
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert ops.mhc_get_device_status() == 0
+        for k in range(n):
+            for key, v in eager[k].items():
+                got = cap[k][key]
+                if v.dtype == torch.bfloat16:
+                    v, got = v.view(torch.int16), got.view(torch.int16)
+                assert torch.equal(v, got), (k, key)
+
+
 # ------------------------------------------------------------------ reciprocal
 
 
