@@ -29,9 +29,10 @@
 // while the CTA streams). The other forms leave the coefficients to a small
 // kernel that reduces the partials.
 //
-// Warps: 0 TMA producer and TMEM owner, 1 MMA issuer, 2-3 idle, 4-11
-// workers (token 32*(warp%4) + lane, so a warp's tokens are its TMEM lane
-// quarter; warps 4-7 take hidden 0-15 of a chunk, 8-11 hidden 16-31), 12-15
+// Warps: 0 TMA producer and TMEM owner, 1 MMA issuer, 2-3 idle (but warp 2
+// of CTA 0, which advances a captured call's flag value), 4-11 workers
+// (token 32*(warp%4) + lane, so a warp's tokens are its TMEM lane quarter;
+// warps 4-7 take hidden 0-15 of a chunk, 8-11 hidden 16-31), 12-15
 // finishers (token 32*(warp%4) + lane). Registers are redistributed per
 // warpgroup with setmaxnreg: 40 + 184 + 184 + 96 per thread, 64,512 of the
 // 65,536 the CTA is launched with (the workers measured 2 % slower at 168,
@@ -893,11 +894,23 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         const int t = q * 32 + lane;
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint64_t pol_out = policy_evict_first();
-        // Item k is published as soon as its accumulator is ready; its layer
-        // input is written one item later, once the tile's other slices have
-        // published too (by then they almost always have).
-        for (int k = 0; k <= n_local; ++k) {
-            if (k < n_local) {
+        // Steps: publish item k (P k) as soon as its accumulator is ready;
+        // write its layer input (L k) once the tile's other slices have
+        // published too. In the order P0 P1 L0 P2 L1 ... P(n-2) L(n-3), an
+        // item's siblings have almost always published by the time of its
+        // L step, so the polls rarely wait (polling right after each P cost
+        // 10 % of a long run). The tail runs L(n-2) P(n-1) L(n-1): L(n-2)
+        // then overlaps the streaming of the last item, and only L(n-1) is
+        // left after its last chunk. Every wait points at an earlier tile or
+        // at items the same wave streams without this CTA, so there is no
+        // cycle. Iteration j runs P(pk) (if pk >= 0), then L(lk) (if lk >= 0);
+        // the decode variants (one item) run P0 L0 in one iteration.
+        const int n_iter = kDecodeMap ? 1 : n_local + 1;
+        for (int j = 0; j < n_iter; ++j) {
+            const int pk = kDecodeMap ? 0 : j < n_local - 1 ? j : (j == n_local ? n_local - 1 : -1);
+            const int lk = kDecodeMap ? 0 : j < n_local ? j - 1 : n_local - 1;
+            if (pk >= 0) {
+                const int k = pk;
                 const int b = k % kAccBufs;
                 const uint32_t ph = (k / kAccBufs) & 1;
                 const Item it = item_of(k, n_slices);
@@ -994,15 +1007,15 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     }
                 }
             }
-            if (!kShifted || k == 0) continue;
+            if (!kShifted || lk < 0) continue;
 
-            // ---- layer input of item kn = k - 1
-            const int kn = k - 1, lb = kn % kLiBufs;
+            // ---- layer input of item kn = lk
+            const int kn = lk, lb = kn % kLiBufs;
             const Item it = item_of(kn, n_slices);
             const long long gt = static_cast<long long>(it.tile) * kTileT + t;
             bool ok = __all_sync(0xffffffffu, !*abort_flag);
             // 32 hidden per chunk; lane l fetches norm weight l of the chunk
-            // (one coalesced load per warp) and the values go round by shuffle
+            // (one coalesced load per warp)
             auto nw_lane = [&](int c) -> float {
                 if (a.norm_w == nullptr) return 0.f;
                 const long long h = chunk_hidden(it.slice, c, n_slices) + lane;
@@ -1014,9 +1027,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             };
             // every chunk's weights (at most 8 chunks) are fetched before the
             // wait for the tile, off the end of a decode call's critical path,
-            // and parked in this warp's shared copy (each lane reads back the
-            // values it wrote), so that no registers are held across the
-            // sums of squares below
+            // and parked in this warp's shared copy, so that no registers are
+            // held across the sums of squares below; the lanes then read them
+            // back as broadcasts, four at a time
             float *nws = red + kNwOff + q * (8 * kChunk);
             {
                 float nwv[8];
@@ -1025,6 +1038,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     if (c < d) nws[c * kChunk + lane] = nwv[c];
+                __syncwarp();
             }
             // every slice of the tile published. The layer RMSNorm needs the
             // flags of this warp's token quarter only: one acquire read per
@@ -1143,7 +1157,6 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             }
             const uint32_t li = tmem_base + lane_off + kLiCol + lb * kLiCols;
             for (int c = 0; c < d; ++c) {
-                const float w_cur = nws[c * kChunk + lane];
                 uint32_t w16[16];
                 if (kDecodeMap) {
                     // the collapse of chunk c sits in its stage's x tile, row t
@@ -1164,13 +1177,20 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {            // the two 16-wide halves
                     uint32_t o[8];
+                    // the half's 16 norm weights, broadcast from the warp's copy
+                    float wv[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 w4 = *reinterpret_cast<const float4 *>(nws + c * kChunk + 16 * hh + 4 * j);
+                        wv[4 * j] = w4.x;
+                        wv[4 * j + 1] = w4.y;
+                        wv[4 * j + 2] = w4.z;
+                        wv[4 * j + 3] = w4.w;
+                    }
 #pragma unroll
                     for (int p = 0; p < 8; ++p) {
                         const uint32_t wd = w16[8 * hh + p];
-                        const int e = 16 * hh + 2 * p;
-                        // every lane takes part in the shuffles
-                        const float w_lo = __shfl_sync(0xffffffffu, w_cur, e);
-                        const float w_hi = __shfl_sync(0xffffffffu, w_cur, e + 1);
+                        const float w_lo = wv[2 * p], w_hi = wv[2 * p + 1];
                         if (a.norm_w != nullptr) {
                             const float lo = __fmul_rn(__fmul_rn(__uint_as_float(wd << 16), rstd_li), w_lo);
                             const float hi =
