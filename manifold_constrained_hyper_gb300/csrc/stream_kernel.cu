@@ -350,10 +350,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         mbar_init(end_full, 1);
         *abort_flag = 0;
         fence_mbar_init();
-        // a single wave (a decode batch) sends its first loads before the
-        // rest of the set-up; a long run of items does better without (the
-        // 8192 x 7168 call measured 5 us slower with it)
-        if (a.fuse_coef)
+        // the shifted form sends its first loads before the rest of the
+        // set-up (the first stage landed ~3.5 us after the kernel started;
+        // 0.4-0.9 us less from 768 to 8192 tokens at hidden 7168); the
+        // unshifted forms keep them in the producer (their register
+        // allocation spilled otherwise)
+        if (kShifted)
             for (int g = 0; g < total && g < kStages; ++g) issue_load(g);
     }
     constexpr uint32_t kTmemCols = kShifted && !kDecodeMap ? 512 : kAccBufs * kAccCols;
@@ -391,11 +393,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         regs_dec_producer();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer
-            // (in a single wave the first kStages loads went out right after
-            // the barriers were initialised)
+            // (in the shifted form the first kStages loads went out right
+            // after the barriers were initialised)
             const uint64_t pol_stream = policy_evict_first();
             int loaded = 0;
-            if (a.fuse_coef)
+            if (kShifted)
                 loaded = total < kStages ? total : kStages;
             else
                 for (; loaded < total && loaded < kStages; ++loaded) issue_load(loaded);
