@@ -381,13 +381,21 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // its workers: in a single wave of items as soon as the tile has
     // published (reduction split into ranges, for latency), otherwise after
     // the CTA's last item (reduction in slice order, as in the
-    // batch-invariant plan)
-    sa.fuse_coef = mode == FUSED_SHIFTED && items <= grid && !invariant;
+    // batch-invariant plan). The unshifted forms do so for a single wave of
+    // one tile whose CTAs have one round of tokens each (kRoundTok), and
+    // then a kernel writes the layer input: at 1 to 128 tokens and hidden
+    // 7168 that took 0.4-2.4 us less than the coefficients kernel between
+    // the two. With several rounds per CTA the in-kernel reduction, which
+    // the layer-input kernel waits for, grows with them; those calls keep
+    // the coefficients kernel.
+    const bool one_round = tiles == 1 && (T + S - 1) / S <= kRoundTok;
+    sa.fuse_coef = items <= grid && !invariant && (mode == FUSED_SHIFTED || one_round);
     sa.coef_end = mode == FUSED_SHIFTED && !sa.fuse_coef;
-    sa.decode_map = sa.fuse_coef && T <= kDecodeMaxTokens && w / kChunk <= kStreamStages
+    sa.decode_map = mode == FUSED_SHIFTED && sa.fuse_coef && T <= kDecodeMaxTokens &&
+                            w / kChunk <= kStreamStages
                         ? (T <= 32 ? 1 : 2)
                         : 0;
-    if (mode == FUSED_SHIFTED) {
+    if (sa.fuse_coef || mode == FUSED_SHIFTED) {
         // Flags hold a value unique to the call. A captured call replays with
         // its launch arguments frozen, so it takes the value from a cell in
         // the workspace (plus one) and advances the cell itself once every
@@ -431,7 +439,8 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     fa.T = T;
     fa.H = H;
     if (mode == FUSED_SHIFTED) return MHC_OK;
-    if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
+    if (!sa.fuse_coef)
+        if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
     return cuda_status(launch_collapse_unshifted(fa, st));
 }
 

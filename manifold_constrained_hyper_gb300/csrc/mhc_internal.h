@@ -94,6 +94,7 @@ struct FinishArgs {
 constexpr int kGridCap = 152;                       // persistent CTAs: one per GB300 SM
 constexpr int kStreamStages = 4;                    // pipeline stages of the streaming kernel
 constexpr int kDecodeMaxTokens = 64;                // most tokens of the decode worker mapping
+constexpr int kRoundTok = 5;                        // single wave: tokens per coefficient round
 constexpr int kMaxSplits = 64;                      // split-K pre: most K splits accepted
 
 size_t stream_smem_bytes();

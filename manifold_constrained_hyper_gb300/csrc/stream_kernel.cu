@@ -66,7 +66,6 @@ constexpr int kMiscOff = kSumsOff + kAccBufs * 2 * 2 * kTileT * 4;
 constexpr int kRedOff = kMiscOff + 64;
 constexpr int kWorkThreads = 256;
 constexpr int kFinThreads = 128;
-constexpr int kRoundTok = 5;                           // tokens per coefficient round
 constexpr int kFinBarrier = 1;                         // named barrier of the finisher warps
 constexpr int kWorkBarrier = 2;                        // named barrier of the worker warps
 constexpr int kRsumOff = kWorkThreads + kFinThreads;   // float offsets within the scratch
@@ -996,8 +995,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 }
                 // publish this quarter of the item to the tile's other slices
                 // (a single wave: the whole item at once, after the four
-                // finisher warps have written, with one flag)
-                if (kShifted) {
+                // finisher warps have written, with one flag; the unshifted
+                // forms publish only then, for the in-kernel coefficients)
+                if (kShifted || a.fuse_coef) {
                     unsigned long long *flag =
                         a.flags + (static_cast<long long>(it.tile) * n_slices + it.slice) * 4;
                     if (a.fuse_coef) {
@@ -1009,9 +1009,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     }
                 }
             }
-            if (!kShifted || lk < 0) continue;
+            if (lk < 0 || (!kShifted && !a.fuse_coef)) continue;
 
-            // ---- layer input of item kn = lk
+            // ---- layer input of item kn = lk (the unshifted forms: only the
+            // wait for the tile, which releases the workers' coefficients)
             const int kn = lk, lb = kn % kLiBufs;
             const Item it = item_of(kn, n_slices);
             const long long gt = static_cast<long long>(it.tile) * kTileT + t;
@@ -1033,7 +1034,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             // held across the sums of squares below; the lanes then read them
             // back as broadcasts, four at a time
             float *nws = red + kNwOff + q * (8 * kChunk);
-            {
+            if (kShifted) {
                 float nwv[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) nwv[c] = c < d ? nw_lane(c) : 0.f;
@@ -1108,6 +1109,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             // the workers may form the coefficients now (also after an abort,
             // so that their wait ends)
             if (a.fuse_coef && lane == 0) mbar_arrive(coef_go);
+            // the unshifted forms' layer input needs this boundary's pre: a
+            // kernel after this one writes it
+            if (!kShifted) continue;
             float rstd_li = 0.f;
             if (a.fuse_coef) {
                 // single wave: the four finisher warps share the reduction. The
@@ -1240,11 +1244,13 @@ cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtenso
         if (e != cudaSuccess) return e;
         opted.fetch_or(bit, std::memory_order_release);
     }
-    if (MODE != FUSED_SHIFTED && MODE != kShiftedDecode && MODE != kShiftedDecodeHalf) {
+    if (MODE != FUSED_SHIFTED && MODE != kShiftedDecode && MODE != kShiftedDecodeHalf &&
+        !a.fuse_coef) {
         kern<<<grid, kThreads, smem, s>>>(res, x, rout, a, n_slices, n_items);
         return cudaGetLastError();
     }
-    // the shifted form's CTAs wait on one another: launch them co-resident
+    // the shifted form's CTAs wait on one another (and the unshifted forms'
+    // when they form the coefficients): launch them co-resident
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);

@@ -74,16 +74,18 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
     S, _ = ops.plan(T, H)
     # the library's internal partials, 25 values per token and slice (24
     # mixes, then the 4H sum of squares), in a block of 128 x 32 floats per
-    # (128-token tile, slice) item: value-major [25][128] in the unshifted
-    # forms; token-major [128][28] when the call is a single wave of items
-    # and the shifted streaming kernel's workers reduce them; otherwise
-    # (shifted, several items per CTA) one 32-float record per token and
-    # slice, [tiles * 128][S][32]
+    # (128-token tile, slice) item: token-major [128][28] when the streaming
+    # kernel's workers reduce them (a single wave of items; for the unshifted
+    # forms only one tile whose CTAs have at most 5 tokens each, one round);
+    # value-major [25][128] in the other unshifted calls; otherwise (shifted,
+    # several items per CTA) one 32-float record per token and slice,
+    # [tiles * 128][S][32]
     tiles = (T + 127) // 128
     sms = min(152, torch.cuda.get_device_properties(0).multi_processor_count)
     raw = ws[: tiles * S * 32 * 128 * 4].view(torch.float32).view(tiles, S, 32 * 128)
     single_wave = tiles * S <= sms and not (params and params.batch_invariant)
-    if mode == "shifted" and single_wave:
+    in_kernel = single_wave and (mode == "shifted" or (tiles == 1 and -(-T // S) <= 5))
+    if in_kernel:
         blk = raw[..., : 128 * 28].reshape(tiles, S, 128, 28)[..., :25].permute(1, 0, 2, 3)
     elif mode == "shifted":
         blk = raw.reshape(tiles * 128, S, 32)[..., :25].permute(1, 0, 2)
