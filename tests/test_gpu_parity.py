@@ -95,6 +95,19 @@ def test_decode_sweep_shifted_h7168(T):
     compare("shifted", g, o, li_ulps=1)
 
 
+@pytest.mark.parametrize("mode", ["unshifted", "pre"])
+@pytest.mark.parametrize("T", [1, 5, 33, 64, 113, 128])
+def test_decode_sweep_unshifted_h7168(mode, T):
+    """Unshifted and pre-only calls of one tile at hidden 7168 (112 slices,
+    at most 2 tokens per CTA): the streaming kernel forms the coefficients
+    and the collapse kernel follows. 113 tokens: one more than the slices,
+    so a CTA has two tokens and others one."""
+    d = synth.make_inputs(**synth.decode_workload(T))
+    g = run_gpu(mode, d)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, d=d)
+
+
 @pytest.mark.parametrize("mode", ["shifted", "unshifted", "pre"])
 @pytest.mark.parametrize("T,H", [(129, 256), (200, 512), (333, 1024), (130, 4096)])
 def test_ragged_tiles(mode, T, H):
