@@ -59,7 +59,7 @@ alg_bytes_stream_kernel = alg_bytes_call
 # workload, from one ncu capture of the current kernel
 # (profiles/boundary_prefill_t8192_h7168_dram.md); empty until the capture of
 # the current kernel is taken. None for other sizes.
-STREAM_KERNEL_TRAFFIC = {(8192, 7168): 598.01e6 + 541.11e6}
+STREAM_KERNEL_TRAFFIC = {(8192, 7168): 598.12e6 + 541.24e6}
 
 
 # ---------------------------------------------------------------- clocks
