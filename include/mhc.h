@@ -125,13 +125,15 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *residual, const float *po
 
 /* Bytes of caller-provided device scratch for mhc_pre / mhc_boundary_fused
  * at (T, H): per-token partial mixes and sums of squares of every hidden
- * slice, and the shifted form's publication flags. 0 when T == 0. It needs
- * no initialisation. Calls may be captured into a CUDA graph (they allocate
- * nothing and never synchronise): a captured shifted call takes its flag
- * value from a cell in the workspace and advances the cell itself, so each
- * replay has its own value and replays may run with new contents in the
- * same buffers (still one kernel per call). Calls that share a
- * workspace must not overlap in time. */
+ * slice, and the publication flags. 0 when T == 0. It needs no
+ * initialisation. Calls may be captured into a CUDA graph (they allocate
+ * nothing and never synchronise). A call whose blocks wait on one another
+ * (every shifted call, and the unshifted calls of at most 128 tokens whose
+ * streaming kernel forms the coefficients) marks its progress with a flag
+ * value; captured, it takes the value from a cell in the workspace and
+ * advances the cell itself, so each replay has its own value and replays
+ * may run with new contents in the same buffers (no extra kernel). Calls
+ * that share a workspace must not overlap in time. */
 size_t mhc_workspace_bytes(int64_t tokens, int hidden);
 
 /*
