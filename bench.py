@@ -55,11 +55,46 @@ def alg_bytes_call(T: int, H: int) -> int:
 alg_bytes_stream_kernel = alg_bytes_call
 
 
-# DRAM bytes (read + write) of one streaming-kernel launch of the 8192 x 7168
-# workload, from one ncu capture of the current kernel
-# (profiles/boundary_prefill_t8192_h7168_dram.md); empty until the capture of
-# the current kernel is taken. None for other sizes.
-STREAM_KERNEL_TRAFFIC = {(8192, 7168): 598.12e6 + 541.24e6}
+def alg_bytes_form(form: str, T: int, H: int) -> int:
+    """Algorithmic bytes of one call of each form (one pass over each tensor,
+    the byte convention of the FlashInfer page's SOL figures): shifted as
+    alg_bytes_call; unshifted fused: no lagged pre in (80 B of coefficients
+    in per token); pre-only: residual in, layer input and 96 B of
+    coefficients out per token. The prepared mixer and the fp32 norm
+    weight once in every form."""
+    per_tok = {"shifted": 20 * H + 192, "unshifted": 20 * H + 176, "pre": 10 * H + 96}[form]
+    return T * per_tok + 388 * H
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one
+# streaming-kernel launch, by (tokens, hidden), from one-pass ncu captures
+# of the full-size workload, each with the hash of the kernel sources it was
+# taken on (source_hash()). A figure whose hash no longer matches the
+# sources being run is not reported: the kernel has changed since.
+STREAM_KERNEL_TRAFFIC = {(8192, 7168): (598.12e6 + 541.24e6, "8e87aaa0f12d1392")}
+KERNEL_SOURCES = ("stream_kernel.cu", "ptx.cuh", "coef.cuh", "mhc_internal.h")
+
+
+def source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the streaming kernel's sources."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "manifold_constrained_hyper_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def stream_kernel_traffic(T: int, H: int):
+    """(bytes per launch or None, note)."""
+    rec = STREAM_KERNEL_TRAFFIC.get((T, H))
+    if rec is None:
+        return None, "no capture of this size"
+    if rec[1] != source_hash():
+        print(f"bench: the DRAM traffic figure for {T}x{H} was captured on other kernel "
+              f"sources ({rec[1]} != {source_hash()}); reporting traffic null", file=sys.stderr)
+        return None, "kernel changed since the capture"
+    return rec[0], f"one-pass ncu capture of this workload, sources {rec[1]}"
 
 
 # ---------------------------------------------------------------- clocks
@@ -245,38 +280,93 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _graph_us(call, n: int, dev) -> float:
+    """Per-call device time of `call` from one replay of a CUDA graph of n calls."""
+    import torch
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n):
+                call(s)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) * 1e3 / n
+
+
+def _boundary_call(form, ins, outs, ws, params=None):
+    """A call of one form on prepared device tensors: (stream -> None)."""
+    from manifold_constrained_hyper_gb300 import ops
+    if form == "pre":
+        o = {k: outs[k] for k in ("layer_input", "pre_out", "post_out", "comb_out")}
+        return lambda st=None: ops.mhc_pre(ins["res"], ins["w"], ins["scale"], ins["base"],
+                                           ins["nw"], params, workspace=ws, stream=st, **o)
+    pl = ins["pl"] if form == "shifted" else None
+    return lambda st=None: ops.mhc_boundary_fused(ins["x"], ins["res"], ins["post"], ins["comb"],
+                                                  ins["w"], ins["scale"], ins["base"], ins["nw"],
+                                                  pl, params, workspace=ws, stream=st, **outs)
+
+
+def _device_inputs(d, dev):
+    import torch
+    from manifold_constrained_hyper_gb300 import ops
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)
+    res = d["residual_dev"] if "residual_dev" in d else bf(d["residual"])
+    x = d["x_dev"] if "x_dev" in d else bf(d["x"])
+    return dict(res=res, x=x, post=f32(d["post"]), comb=f32(d["comb"]), pl=f32(d["pre_lag"]),
+                scale=f32(d["scale"]), base=f32(d["base"]), nw=f32(d["norm_w"]),
+                w=ops.mhc_prepare_weight(f32(d["fn"])))
+
+
+def _device_outputs(T, H, res, dev):
+    import torch
+    return dict(residual_out=torch.empty_like(res),
+                layer_input=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                pre_out=torch.empty(T, 4, device=dev), post_out=torch.empty(T, 4, device=dev),
+                comb_out=torch.empty(T, 4, 4, device=dev))
+
+
 def measure_decode(dev, token_counts=None):
-    """Latency of one shifted call at the decode batch sizes, hidden H: per
-    call from a CUDA graph of 100 calls (launch cost amortised, L2 warm as in
-    a decode loop), eager per-call CUDA events with L2 warm, and eager with a
-    256 MB buffer written before each call (L2 cold). Inputs of each size
-    are the seeded decode workload (hidden 7168, seed 1000 + T)."""
+    """Latency of one call at the decode batch sizes, hidden 7168 (the seeded
+    decode workload, seed 1000 + T):
+    * graph / graph_unshifted / graph_pre: per call from a CUDA graph of 100
+      calls of the shifted, unshifted fused and pre-only forms (launch cost
+      amortised, L2 warm as in a decode loop);
+    * eager_warm: device time of one eager shifted call with L2 warm, its
+      events and the call enqueued behind a short GPU sleep so that they run
+      back to back (the host's enqueue time is not counted);
+    * eager_cold_l2: the same after a 256 MB buffer was written (L2 cold);
+    * host_us_per_call: host time of one eager shifted call through the
+      Python binding and, apart, through the C entry point alone (ctypes
+      with its arguments prebuilt), mean over 200 calls."""
+    import ctypes as ct
     import torch
     from manifold_constrained_hyper_gb300 import ops, synth
     token_counts = token_counts or synth.DECODE_TOKENS
     H = synth.DECODE_HIDDEN
     scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)
-    out = {"hidden": H, "unit": "us/call", "graph": {}, "eager_warm": {}, "eager_cold_l2": {},
-           "slices": {}, "waves": {}}
+    out = {"hidden": H, "unit": "us/call", "graph": {}, "graph_unshifted": {}, "graph_pre": {},
+           "eager_warm": {}, "eager_cold_l2": {}, "host_us_per_call": {}, "slices": {},
+           "waves": {}}
     sms = min(152, torch.cuda.get_device_properties(dev).multi_processor_count)
     for T in token_counts:
         cfg = synth.decode_workload(T)
         d = synth.make_inputs(cfg["T"], cfg["H"], seed=cfg["seed"])
-        res, x = bf(d["residual"]), bf(d["x"])
-        post, comb, pl = f32(d["post"]), f32(d["comb"]), f32(d["pre_lag"])
-        scale, base, nw = f32(d["scale"]), f32(d["base"]), f32(d["norm_w"])
-        w = ops.mhc_prepare_weight(f32(d["fn"]))
-        outs = dict(residual_out=torch.empty_like(res),
-                    layer_input=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
-                    pre_out=torch.empty(T, 4, device=dev), post_out=torch.empty(T, 4, device=dev),
-                    comb_out=torch.empty(T, 4, 4, device=dev),
-                    workspace=torch.empty(ops.workspace_bytes(T, H), dtype=torch.uint8, device=dev))
-
-        def call():
-            ops.mhc_boundary_fused(x, res, post, comb, w, scale, base, nw, pl, **outs)
-
+        ins = _device_inputs(d, dev)
+        outs = _device_outputs(T, H, ins["res"], dev)
+        ws = torch.empty(ops.workspace_bytes(T, H), dtype=torch.uint8, device=dev)
+        call = _boundary_call("shifted", ins, outs, ws)
         for _ in range(5):
             call()
         torch.cuda.synchronize()
@@ -286,48 +376,83 @@ def measure_decode(dev, token_counts=None):
             a.record()
             b.record()
         torch.cuda.synchronize()
-        for a, b in ev:
-            a.record()
-            call()
-            b.record()
-        torch.cuda.synchronize()
-        warm = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
-        cold = []
-        for a, b in ev[:20]:
-            scrub.add_(1)
+        warm, cold = [], []
+        for i, (a, b) in enumerate(ev):
+            if i < 20:
+                scrub.add_(1)
+            torch.cuda._sleep(100_000)               # the GPU waits while the host enqueues
             a.record()
             call()
             b.record()
             torch.cuda.synchronize()
-            cold.append(a.elapsed_time(b) * 1e3)
-        s = torch.cuda.Stream(device=dev)
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            call()
+            (cold if i < 20 else warm).append(a.elapsed_time(b) * 1e3)
+        # host time per call: Python binding, then the C entry point alone
+        lib = ops.load()
+        p = ops.Params().c()
+        cst = ops._stream(None, ins["res"].device)
+        args = [ins["x"].data_ptr(), ins["res"].data_ptr(), ins["post"].data_ptr(),
+                ins["comb"].data_ptr(), ins["pl"].data_ptr(), ins["w"].data_ptr(),
+                ins["scale"].data_ptr(), ins["base"].data_ptr(), ins["nw"].data_ptr(), 0,
+                ct.byref(p), T, H, outs["residual_out"].data_ptr(), outs["layer_input"].data_ptr(),
+                outs["pre_out"].data_ptr(), outs["post_out"].data_ptr(), outs["comb_out"].data_ptr(),
+                ws.data_ptr(), ws.numel(), cst]
+        host = {}
+        for kind in ("python", "c_entry"):
             torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=s):
-                for _ in range(100):
+            t0 = time.perf_counter()
+            for _ in range(200):
+                if kind == "python":
                     call()
-        torch.cuda.synchronize()
-        g.replay()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        S, _ = ops.plan(T, H)
+                else:
+                    lib.mhc_boundary_fused(*args)
+            host[kind] = (time.perf_counter() - t0) / 200 * 1e6
+            torch.cuda.synchronize()
+        out["host_us_per_call"][str(T)] = host
         key = str(T)
-        out["graph"][key] = a.elapsed_time(b) * 1e3 / 100
-        out["eager_warm"][key] = warm
+        out["graph"][key] = _graph_us(call, 100, dev)
+        for form in ("unshifted", "pre"):
+            out["graph_" + form][key] = _graph_us(_boundary_call(form, ins, outs, ws), 100, dev)
+        out["eager_warm"][key] = statistics.median(warm)
         out["eager_cold_l2"][key] = statistics.median(cold)
+        S, _ = ops.plan(T, H)
         out["slices"][key] = S
         out["waves"][key] = -(-((T + 127) // 128 * S) // sms)
-        del g
     if ops.mhc_get_device_status() != 0:
         raise RuntimeError("device-side wait timed out during the decode sweep")
     return out
+
+
+def measure_forms(dev):
+    """Every form of the boundary at the mid-batch (512 x 7168) and prefill
+    (8192 x 7168) sizes, and the stress workload (1024 x 4096, residual ~
+    N(0, 8) with outliers, base ~ N(0, 4), 20 Sinkhorn iterations): per call
+    from a CUDA graph of calls (inputs larger than L2 at 8192 tokens; at the
+    smaller sizes the inputs stay L2-resident between calls, as in a layer
+    loop that reuses its buffers), GB/s over each form's algorithmic bytes
+    (alg_bytes_form) and its fraction of the measured copy bandwidth."""
+    import torch
+    from manifold_constrained_hyper_gb300 import ops, synth
+    peak, _ = measured_peaks()
+    res_out = {"unit": "us/call", "peak_gbs": peak, "cases": {}}
+    cases = [("mid_t512_h7168", 50), ("prefill_t8192_h7168", 10), ("stress_t1024_h4096", 20)]
+    for name, n in cases:
+        cfg = dict(synth.WORKLOADS[name])
+        T, H, seed = cfg.pop("T"), cfg.pop("H"), cfg.pop("seed")
+        d = synth.make_inputs_device(T, H, seed, dev, **cfg)
+        ins = _device_inputs(d, dev)
+        outs = _device_outputs(T, H, ins["res"], dev)
+        ws = torch.empty(ops.workspace_bytes(T, H), dtype=torch.uint8, device=dev)
+        for form in ("shifted", "unshifted", "pre"):
+            us = _graph_us(_boundary_call(form, ins, outs, ws), n, dev)
+            gbs = alg_bytes_form(form, T, H) / us / 1e3
+            res_out["cases"][f"{name}/{form}"] = {
+                "tokens": T, "hidden": H, "us": us, "tokens_per_s": T / us * 1e6, "gbps": gbs,
+                "frac_of_peak": gbs / peak, "graph_calls": n}
+        del d, ins, outs, ws
+        torch.cuda.empty_cache()
+    if ops.mhc_get_device_status() != 0:
+        raise RuntimeError("device-side wait timed out while timing the forms")
+    return res_out
 
 
 def measure_split_k(dev):
@@ -537,14 +662,14 @@ def run_ours(args):
                "single_thread": {"value": n1 / s1, "cores": 1,
                                  "sample": f"{n1} tokens in {s1:.1f} s"}}
 
-    decode = None
+    decode = forms = split_k = None
     if not args.no_decode:
         decode = measure_decode(dev)
-    split_k = None
-    if not args.no_decode:
+        forms = measure_forms(dev)
         split_k = measure_split_k(dev)
 
     S, sw = ops.plan(T, H)
+    traffic, traffic_note = stream_kernel_traffic(T, H)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -559,12 +684,13 @@ def run_ours(args):
         "achieved_frac_of_peak": gbps_call / peak,
         "kernel_ms": {"stream": stream_ms},
         "roofline": {"bound": "hbm", "kernel": "stream_kernel", "achieved": ach, "peak": peak,
-                     "unit": "GB/s", "frac": ach / peak, "traffic": STREAM_KERNEL_TRAFFIC.get((T, H)),
-                     "peak_source": peak_kind},
+                     "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
+                     "traffic_source": traffic_note, "peak_source": peak_kind},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": K,
         "decode": decode,
+        "forms": forms,
         "pre_split_k": split_k,
         "clocks": clk.summary(),
     }
@@ -585,7 +711,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true",
-                    help="skip the decode-latency sweep (1-64 tokens) and the split-K pre timings")
+                    help="skip the decode-latency sweep (1-64 tokens), the other forms and "
+                         "workloads, and the split-K pre timings")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-tokens", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=0,

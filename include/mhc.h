@@ -101,6 +101,13 @@ size_t mhc_weight_bytes(int hidden);
  *     ((c*4 + s)*48 + r)*32 + 8*((e/8) ^ ((r/2) % 4)) + (e % 8),
  * i.e. per (chunk, stream) a 48 x 64-byte tile, K-major, in the 64-byte
  * swizzled order the tensor cores read from shared memory.
+ * This layout deliberately departs from the page's prepared weight, which
+ * gathers the same hi/lo parts into register fragments of the warp-level
+ * m16n8k16 MMA ([16 slices, k16 steps, 3 m16 tiles, 32 lanes, 4] int32):
+ * here the 5th-generation tensor cores read both operands from shared
+ * memory, so each (chunk, stream) tile lands there with one bulk copy,
+ * already in the swizzled order their descriptors expect. The rounding and
+ * the split are the page's, value for value.
  * Inputs must be finite (NaN payloads are not preserved by the rounding).
  */
 mhc_status mhc_prepare_weight(const float *fn, int hidden, void *weight, void *stream);
@@ -133,7 +140,9 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *residual, const float *po
  * value; captured, it takes the value from a cell in the workspace and
  * advances the cell itself, so each replay has its own value and replays
  * may run with new contents in the same buffers (no extra kernel). Calls
- * that share a workspace must not overlap in time. */
+ * that share a workspace must not overlap in time. The cell sits at the
+ * start of the workspace whatever the call's shape, so calls of different
+ * shapes, eager or captured, may share one workspace sized for the largest. */
 size_t mhc_workspace_bytes(int64_t tokens, int hidden);
 
 /*
@@ -170,6 +179,14 @@ mhc_status mhc_pre(const uint16_t *residual, const void *weight, const float *sc
  * the residual), or NULL (unshifted form: it collapses with this boundary's
  * own pre_out, which re-reads the updated residual).
  * Other arguments as in mhc_post and mhc_pre. residual_out may be == residual.
+ * Limits of the shifted form: its blocks wait on one another within one
+ * launch, so every hidden slice of a 128-token tile must be resident at
+ * once, and an item's collapse must fit its tensor-memory buffer. H / 32
+ * must therefore have a divisor d <= 8 with H / (32 d) <= 152 (slices of d
+ * chunks of 32, at most one per streaming multiprocessor of a GB300): every
+ * multiple of 256 up to 38912 qualifies (7168: 28 slices of 256), H = 65536
+ * or 32 * 157 does not. Other H return MHC_ERR_UNSUPPORTED before anything
+ * is enqueued. The unshifted form has no such limit.
  */
 mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual,
                               const float *post, const float *comb,

@@ -167,10 +167,14 @@ void plan(long long T, int H, int *n_slices, int *slice_w) {
     *slice_w = best_d * kChunk;
 }
 
-// Workspace: per-item partial blocks [tiles][S] of 128 x 32 fp32, then (each 256-byte
-// aligned) the shifted form's per-slice collapse sums [S][T] fp32, its
-// publication flags [tiles][S][4] u64, and the u64 epoch cell that a call
-// being captured into a CUDA graph takes its flag value from.
+// Workspace: first a 256-byte area holding the u64 epoch cell that a call
+// being captured into a CUDA graph takes its flag value from (at offset 0
+// whatever the call's shape, so that calls of different shapes sharing a
+// workspace never overwrite it with a flag word, nor read a flag as it),
+// then per-item partial blocks [tiles][S] of 128 x 32 fp32, then (each
+// 256-byte aligned) the shifted form's per-slice collapse sums [S][T] fp32
+// and its publication flags [tiles][S][4] u64.
+constexpr size_t kCellBytes = 256;
 size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 size_t partials_bytes(long long T, int S) {
     const size_t tiles = static_cast<size_t>((T + kTileT - 1) / kTileT);
@@ -186,7 +190,7 @@ size_t flags_bytes(long long T, int S) {
 }
 
 size_t workspace_layout_bytes(long long T, int S) {
-    return partials_bytes(T, S) + ssql_bytes(T, S) + flags_bytes(T, S) + 256;
+    return kCellBytes + partials_bytes(T, S) + ssql_bytes(T, S) + flags_bytes(T, S);
 }
 
 // Enough for the plan of either mode (default and batch-invariant).
@@ -347,15 +351,16 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.comb = comb;
     sa.pre_lag = pre_lag;
     sa.weight = static_cast<const uint8_t *>(weight);
-    sa.partials = static_cast<float *>(workspace);
+    uint8_t *const ws8 = static_cast<uint8_t *>(workspace);
+    sa.partials = reinterpret_cast<float *>(ws8 + kCellBytes);
     sa.status = dev->status;
     sa.T = T;
     sa.H = H;
     sa.slice_w = w;
     sa.timeout_ns = g_timeout_ns.load();
-    sa.ssql = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + partials_bytes(T, S));
-    sa.flags = reinterpret_cast<unsigned long long *>(static_cast<uint8_t *>(workspace) +
-                                                      partials_bytes(T, S) + ssql_bytes(T, S));
+    sa.ssql = reinterpret_cast<float *>(ws8 + kCellBytes + partials_bytes(T, S));
+    sa.flags = reinterpret_cast<unsigned long long *>(ws8 + kCellBytes + partials_bytes(T, S) +
+                                                      ssql_bytes(T, S));
     sa.epoch = 0;
     sa.epoch_cell = nullptr;
     sa.bump_cell = 0;
@@ -406,10 +411,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
         cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
         if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MHC_ERR_CUDA;
         if (cap == cudaStreamCaptureStatusActive) {
-            auto *cell = reinterpret_cast<unsigned long long *>(
-                static_cast<uint8_t *>(workspace) + partials_bytes(T, S) + ssql_bytes(T, S) +
-                flags_bytes(T, S));
-            sa.epoch_cell = cell;
+            sa.epoch_cell = reinterpret_cast<unsigned long long *>(ws8);
             sa.bump_cell = sa.fuse_coef && tiles == 1;
             sa.bump_poll = !sa.bump_cell;
         } else {
@@ -426,7 +428,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     }
 
     FinishArgs fa;
-    fa.partials = static_cast<const float *>(workspace);
+    fa.partials = reinterpret_cast<const float *>(ws8 + kCellBytes);
     fa.n_slices = S;
     fa.coef = coef_args(scale, base, params);
     fa.norm_w = norm_w;

@@ -1,6 +1,7 @@
 // mhc_boundary_fused for callers that cannot allocate device memory: the
 // per-slice partials live in a fixed array in the library's own device
 // memory instead of a caller workspace. Nothing here allocates.
+#include <atomic>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -15,12 +16,14 @@ constexpr int kMaxDevices = 64;
 // Every GPU that loads the library holds this array until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// Device address of the array, looked up once per device. In host code the
-// symbol itself is only a host-side stand-in, never a device address.
+// Device address of the array, looked up per device. In host code the
+// symbol itself is only a host-side stand-in, never a device address. Only a
+// successful lookup is kept: a lookup that failed (made during a stream
+// capture, say, or before the device's context was ready) is retried by the
+// next call instead of failing every later call on that device.
 struct ScratchSlot {
-    std::once_flag once;
-    void *ptr = nullptr;
-    cudaError_t err = cudaSuccess;
+    std::atomic<void *> ptr{nullptr};
+    std::mutex m;
 };
 ScratchSlot g_slots[kMaxDevices];
 
@@ -28,11 +31,21 @@ mhc_status scratch_of_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MHC_ERR_CUDA;
     ScratchSlot &s = g_slots[dev];
-    std::call_once(s.once, [&] {
-        s.err = cudaGetSymbolAddress(&s.ptr, g_noalloc_scratch);
-    });
-    if (s.err != cudaSuccess || s.ptr == nullptr) return MHC_ERR_CUDA;
-    *out = s.ptr;
+    void *p = s.ptr.load(std::memory_order_acquire);
+    if (p == nullptr) {
+        std::lock_guard<std::mutex> lock(s.m);
+        p = s.ptr.load(std::memory_order_relaxed);
+        if (p == nullptr) {
+            void *q = nullptr;
+            if (cudaGetSymbolAddress(&q, g_noalloc_scratch) != cudaSuccess || q == nullptr) {
+                cudaGetLastError();   // clear the error this lookup left behind
+                return MHC_ERR_CUDA;
+            }
+            s.ptr.store(q, std::memory_order_release);
+            p = q;
+        }
+    }
+    *out = p;
     return MHC_OK;
 }
 

@@ -12,8 +12,9 @@ with the shapes and value distributions of the workloads it is quoted on:
   size 4 (Birkhoff), so its rows and columns sum to 1;
 * previous boundary's ``pre_lag [T, 4]`` = 1e-6 + U(0, 1);
 * mixer ``fn [24, 4H]`` fp32 ~ N(0, 1/sqrt(4H)) (standard deviation);
-* ``scale = (0.5, 0.5, 0.5)``, ``base [24]`` ~ N(0, base_std),
-  ``norm_w [H]`` fp32 = 1 + N(0, 0.02).
+* ``scale = (0.5, 0.5, 0.5)`` unless given (the per-group scales of pre,
+  post and comb), ``base [24]`` ~ N(0, base_std), ``norm_w [H]`` fp32 =
+  1 + N(0, 0.02).
 
 Everything comes from one ``torch.Generator('cpu')`` seeded with ``seed`` and
 is returned as numpy arrays (bf16 as ``uint16`` bit patterns) so that the CUDA
@@ -53,7 +54,8 @@ def _bf16_bits(t: torch.Tensor) -> np.ndarray:
 
 def make_inputs(T: int, H: int, seed: int, *, residual_std: float = 1.0,
                 outlier_frac: float = 0.0, outlier_mult: float = 100.0,
-                base_std: float = 0.1, with_fn: bool = True) -> dict:
+                base_std: float = 0.1, with_fn: bool = True,
+                scale=(0.5, 0.5, 0.5)) -> dict:
     """All inputs of one boundary call (see the module docstring)."""
     g = torch.Generator("cpu").manual_seed(int(seed))
     res = torch.randn(T, 4, H, generator=g, dtype=torch.float32) * residual_std
@@ -61,12 +63,12 @@ def make_inputs(T: int, H: int, seed: int, *, residual_std: float = 1.0,
         mask = torch.rand(T, 4, H, generator=g) < outlier_frac
         res = torch.where(mask, res * outlier_mult, res)
     x = torch.randn(T, H, generator=g, dtype=torch.float32)
-    return _finish(g, T, H, res, x, base_std, with_fn)
+    return _finish(g, T, H, res, x, base_std, with_fn, scale)
 
 
 def make_inputs_device(T: int, H: int, seed: int, device, *, residual_std: float = 1.0,
                        outlier_frac: float = 0.0, outlier_mult: float = 100.0,
-                       base_std: float = 0.1) -> dict:
+                       base_std: float = 0.1, scale=(0.5, 0.5, 0.5)) -> dict:
     """Same recipe for large workloads: residual and x are drawn on `device`
     by a generator seeded with `seed` and stay there as bf16 tensors
     (``residual_dev``, ``x_dev``); the small tensors come from a CPU generator
@@ -80,14 +82,14 @@ def make_inputs_device(T: int, H: int, seed: int, device, *, residual_std: float
         res = torch.where(mask, res * outlier_mult, res)
     x = torch.randn(T, H, generator=gd, dtype=torch.float32, device=device)
     g = torch.Generator("cpu").manual_seed(int(seed) + 1)
-    out = _finish(g, T, H, None, None, base_std, True)
+    out = _finish(g, T, H, None, None, base_std, True, scale)
     out["residual_dev"] = res.to(torch.bfloat16)
     del res
     out["x_dev"] = x.to(torch.bfloat16)
     return out
 
 
-def _finish(g, T, H, res, x, base_std, with_fn):
+def _finish(g, T, H, res, x, base_std, with_fn, scale):
     post = torch.rand(T, 4, generator=g, dtype=torch.float32) * 2.0
     # Birkhoff: convex weights from normalised exponential draws
     e = -torch.log(torch.rand(T, 24, generator=g, dtype=torch.float64).clamp_min(1e-300))
@@ -102,7 +104,7 @@ def _finish(g, T, H, res, x, base_std, with_fn):
         K = 4 * H
         out["fn"] = (torch.randn(24, K, generator=g, dtype=torch.float32)
                      * (1.0 / np.sqrt(K))).numpy()
-        out["scale"] = np.array([0.5, 0.5, 0.5], np.float32)
+        out["scale"] = np.array(scale, np.float32).reshape(3)
         out["base"] = (torch.randn(24, generator=g, dtype=torch.float32) * base_std).numpy()
         out["norm_w"] = (1.0 + torch.randn(H, generator=g, dtype=torch.float32) * 0.02).numpy()
     return out

@@ -12,7 +12,11 @@ from manifold_constrained_hyper_gb300 import ops
 MODES = {"pre": orc.MODE_PRE_ONLY, "unshifted": orc.MODE_FUSED_UNSHIFTED,
          "shifted": orc.MODE_FUSED_SHIFTED}
 
-# Tolerances (derivation in DESIGN.md "Parity bar"):
+# Tolerances. Coefficients: 1e-5 relative (the fp32 arithmetic of sigmoid,
+# softmax and a 20-step Sinkhorn on both sides, with libm's and CUDA's exp,
+# leaves a few fp32 ulps), plus 1e-7 absolute for values near zero. Mixes:
+# 1e-5 of the larger of |mix| and the 2-norm of its 4H terms (a mix near zero
+# is a sum that cancelled, whose error scales with its terms, not itself).
 COEF_RTOL, COEF_ATOL = 1e-5, 1e-7      # pre, post, comb
 MIX_RTOL = 1e-5                         # |g - o| <= 1e-5 * max(|o|, ||terms||_2)
 
@@ -82,7 +86,8 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
     # [tiles * 128][S][32]
     tiles = (T + 127) // 128
     sms = min(152, torch.cuda.get_device_properties(0).multi_processor_count)
-    raw = ws[: tiles * S * 32 * 128 * 4].view(torch.float32).view(tiles, S, 32 * 128)
+    # (the partials start 256 bytes into the workspace, after the epoch cell)
+    raw = ws[256: 256 + tiles * S * 32 * 128 * 4].view(torch.float32).view(tiles, S, 32 * 128)
     single_wave = tiles * S <= sms and not (params and params.batch_invariant)
     in_kernel = single_wave and (mode == "shifted" or (tiles == 1 and -(-T // S) <= 5))
     if in_kernel:
@@ -143,6 +148,40 @@ def oracle_layer_input_given_pre(mode: str, d: dict, pre: np.ndarray, norm="f32"
     return run_oracle("shifted", dd, norm, params, rows)["layer_input"]
 
 
+def _f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _ulp(v: np.ndarray) -> np.ndarray:
+    """One bf16 ulp at the magnitude of v (8 significant bits)."""
+    return np.ldexp(1.0, np.frexp(np.maximum(np.abs(v), 2.0 ** -126))[1] - 8)
+
+
+def _unshifted_li_excess(mode, d, g, o, li_gpu, norm, rows):
+    """Largest ratio of |out_gpu - out_oracle| to the element's derived bound
+    (see compare): <= 1 means every element is within its bound."""
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    stream = host_bits(g["residual_out_dev"]) if mode == "unshifted" else sel(d["residual"])
+    if mode == "unshifted":
+        stream = sel(stream)
+    r = _f64(stream)                                             # [t, 4, H]
+    p_o = o["pre"].astype(np.float64)
+    p_g = sel(g["pre"]).astype(np.float64)
+    E = np.einsum("tj,tjh->th", np.abs(p_g - p_o), np.abs(r))
+    li_o = np.einsum("tj,tjh->th", p_o, r)
+    if norm is None:
+        scale = np.ones_like(li_o)
+    else:
+        w = d["norm_w"].astype(np.float64)
+        if norm == "bf16":
+            w = _f64(orc.f32_to_bf16(d["norm_w"]))
+        scale = o["rstd_li"].astype(np.float64)[:, None] * np.abs(w)[None, :]
+    out_o = _f64(o["layer_input"])
+    bound = 2 * _ulp(out_o) + (E + _ulp(li_o)) * scale
+    err = np.abs(_f64(li_gpu) - out_o)
+    return float(np.max(err / bound)) if err.size else 0.0
+
+
 def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: bool = True,
             d: dict | None = None, norm="f32", params=None):
     """Element-wise comparison of GPU outputs (optionally the token `rows`)
@@ -152,9 +191,16 @@ def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: boo
     1 bf16 ulp against the oracle. Unshifted / pre-only, the collapse uses
     this boundary's pre, which the two sides form in different summation
     orders (checked separately at 1e-5); where sum_j pre_j r_j cancels, that
-    difference is amplified without bound in ulps, so the bar is 1 ulp
-    against the oracle's layer input computed from the GPU's own pre, and at
-    least 99.9 % of elements within 1 ulp of the independent oracle."""
+    difference is amplified in ulps. So the bar there is: 1 ulp against the
+    oracle's layer input computed from the GPU's own pre; at least 99.9 % of
+    elements within 1 ulp of the independent oracle; and every element
+    within a bound derived from the pre difference: with
+    E = sum_j |pre_gpu_j - pre_oracle_j| |r_j| (how far the two collapse
+    sums can be apart before rounding), |out_gpu - out_oracle| <=
+    2 ulp(out) + (E + ulp(li)) * rstd_li * |norm_w|, li = sum_j pre_j r_j
+    (the roundings of li and of the output on each side, and the sum's
+    spread carried through the normalisation). The count of elements
+    beyond 1 ulp and the largest distance are recorded in the stats."""
     sel = (lambda a: a) if rows is None else (lambda a: a[rows])
     stats = {}
     if mode != "pre":
@@ -164,6 +210,7 @@ def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: boo
     du = bf16_ulp_diff(li, o["layer_input"])
     stats["li_max_ulp"] = int(du.max()) if du.size else 0
     stats["li_frac_exact"] = float(np.mean(du == 0)) if du.size else 1.0
+    stats["li_n_beyond_1ulp"] = int(np.sum(du > 1))
     if mode == "shifted":
         assert stats["li_max_ulp"] <= li_ulps, stats
     else:
@@ -173,6 +220,9 @@ def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: boo
         dc = bf16_ulp_diff(li, ref)
         stats["li_max_ulp_given_pre"] = int(dc.max()) if dc.size else 0
         assert stats["li_max_ulp_given_pre"] <= 1, stats
+        over = _unshifted_li_excess(mode, d, g, o, li, norm, rows)
+        stats["li_max_over_bound"] = over
+        assert over <= 1.0, stats
     for k in ("pre", "post", "comb"):
         gv, ov = sel(g[k]).astype(np.float64), o[k].astype(np.float64)
         err = np.abs(gv - ov)

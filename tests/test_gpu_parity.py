@@ -79,8 +79,14 @@ def test_post_in_place_and_subnormals():
 # ------------------------------------------------------------------ boundary
 
 
-def test_tiny_t4_h256_all_modes():
-    d = synth.workload_inputs("tiny_t4_h256")
+# distinct per-group scales (pre, post, comb): a swapped group index on
+# either side would show here
+DISTINCT_SCALES = (0.25, 1.5, 3.0)
+
+
+@pytest.mark.parametrize("scale", [(0.5, 0.5, 0.5), DISTINCT_SCALES])
+def test_tiny_t4_h256_all_modes(scale):
+    d = synth.workload_inputs("tiny_t4_h256", scale=scale)
     for mode in ("shifted", "unshifted", "pre"):
         g = run_gpu(mode, d)
         o = run_oracle(mode, d)
@@ -93,6 +99,17 @@ def test_decode_sweep_shifted_h7168(T):
     g = run_gpu("shifted", d)
     o = run_oracle("shifted", d)
     compare("shifted", g, o, li_ulps=1)
+
+
+@pytest.mark.parametrize("mode", ["shifted", "unshifted", "pre"])
+@pytest.mark.parametrize("T", [1, 64])
+def test_decode_distinct_scales_h7168(mode, T):
+    """The single-wave forms, whose coefficients come from the 16-lane
+    routine, with distinct per-group scales."""
+    d = synth.make_inputs(**synth.decode_workload(T), scale=DISTINCT_SCALES)
+    g = run_gpu(mode, d)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, d=d)
 
 
 @pytest.mark.parametrize("mode", ["unshifted", "pre"])
@@ -145,9 +162,10 @@ def test_shifted_several_items_per_cta(T, H):
     compare("shifted", g, o, d=d)
 
 
+@pytest.mark.parametrize("scale", [(0.5, 0.5, 0.5), DISTINCT_SCALES])
 @pytest.mark.parametrize("mode", ["pre", "unshifted", "shifted"])
-def test_mid_batch_t512_h7168(mode):
-    d = synth.workload_inputs("mid_t512_h7168")
+def test_mid_batch_t512_h7168(mode, scale):
+    d = synth.workload_inputs("mid_t512_h7168", scale=scale)
     g = run_gpu(mode, d)
     o = run_oracle(mode, d)
     compare(mode, g, o, d=d)

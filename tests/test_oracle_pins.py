@@ -494,3 +494,206 @@ def test_oracle_reproduces_the_golden_fixture():
     assert set(got) == set(want)
     for k in got:
         assert np.array_equal(got[k].view(np.uint8), np.ascontiguousarray(want[k]).view(np.uint8)), k
+
+
+# ---------------------------------------------------------------- orientation, iteration
+# count, scale groups and the whole op, against float64 references written
+# from the pages ("mhc_boundary": MhcBoundaryKernel.coefficients, sinkhorn,
+# col_normalize) in tests/brute64.py, which shares no code with the oracle.
+
+from tests import brute64  # noqa: E402
+
+
+def _zero_mixer(base, iters, scale=(0.5, 0.5, 0.5), T=1, H=32):
+    """Pre-only boundary with fn = 0: every mix is 0, so the logits are the
+    base values exactly, whatever rstd and scale are."""
+    res = np.zeros((T, 4, H), np.uint16)
+    return orc.boundary(orc.MODE_PRE_ONLY, res, np.zeros((24, 4 * H), np.float32),
+                        np.asarray(scale, np.float32), np.asarray(base, np.float32), None,
+                        params=orc.OracleParams(sinkhorn_iters=iters))
+
+
+@pytest.mark.parametrize("iters", [1, 2, 20])
+def test_comb_orientation_closed_form(iters):
+    """Logit (i, k) is base[8 + 4i + k] and comb[i][k] is its entry: with a
+    large logit at k = (i + 1) mod 4 of every row i (a non-symmetric
+    pattern), softmax and Sinkhorn give nearly that shifted permutation
+    matrix, and its transpose gets nearly nothing."""
+    base = np.zeros(24, np.float32)
+    for i in range(4):
+        base[8 + 4 * i + (i + 1) % 4] = 12.0
+    c = _zero_mixer(base, iters)["comb"][0].astype(np.float64)
+    for i in range(4):
+        k = (i + 1) % 4
+        assert c[i, k] > 0.999, (i, k, c)
+        assert c[k, i] < 1e-3, (k, i, c)                # the transposed entry
+        assert abs(c[i].sum() - c[i, k]) < 1e-3
+
+
+@pytest.mark.parametrize("iters", [1, 2, 5, 20])
+def test_softmax_sinkhorn_matches_float64_on_non_symmetric_logits(iters):
+    """Random non-symmetric logits (zero mixer, logits = base): the oracle's
+    comb equals a float64 row softmax (plus eps), one column normalisation
+    and iters - 1 (row, column) normalisations, and pre / post equal
+    sigmoid(base) + eps and 2 sigmoid(base). The float64 results one
+    iteration fewer or more differ from it well beyond the tolerance (for
+    the small counts, before Sinkhorn has converged), so the iteration count
+    and the order of the row and column steps are pinned."""
+    rng = np.random.default_rng(1000 + iters)
+    for trial in range(8):
+        base = rng.normal(0.0, 2.0, 24).astype(np.float32)
+        out = _zero_mixer(base, iters)
+        lg = base[8:].astype(np.float64).reshape(4, 4)
+        assert not np.allclose(lg, lg.T)
+        want = brute64.softmax_sinkhorn(lg, iters, 1e-6)
+        got = out["comb"][0].astype(np.float64)
+        assert np.allclose(got, want, rtol=2e-6, atol=1e-9), (iters, trial)
+        if iters <= 5:
+            for other in (iters - 1, iters + 1):
+                if other < 1:
+                    continue
+                alt = brute64.softmax_sinkhorn(lg, other, 1e-6)
+                assert np.max(np.abs(alt - want)) > 1e-4, (iters, other)
+            # a softmax over the other index (columns) gives another matrix
+            alt_t = brute64.softmax_sinkhorn(lg.T, iters, 1e-6).T
+            assert np.max(np.abs(alt_t - want)) > 1e-3
+        b = base.astype(np.float64)
+        assert np.allclose(out["pre"][0], brute64.sigmoid(b[:4]) + 1e-6, rtol=3e-7, atol=0)
+        assert np.allclose(out["post"][0], 2 * brute64.sigmoid(b[4:8]), rtol=3e-7, atol=0)
+
+
+def test_scale_groups_closed_form():
+    """scale[0] multiplies the pre group (mixes 0-3), scale[1] the post group
+    (4-7) and scale[2] every comb logit (8-23). A residual with one nonzero
+    value (1.0 at stream 0, hidden 0) and a mixer whose column 0 holds
+    distinct TF32-exact values a_n makes mix[n] = a_n exactly and the sum of
+    squares 1; with scale = (0.25, 1.5, 3.0) every group is then checked
+    against its float64 closed form (a swapped group index changes the
+    results by orders of magnitude more than the tolerance)."""
+    T, H = 1, 32
+    K = 4 * H
+    res = np.zeros((T, 4, H), np.uint16)
+    res[0, 0, 0] = 0x3F80                                  # 1.0
+    # |a| <= 0.25 keeps every pre-activation moderate (|v| <= 9 with rstd ~ 11.3
+    # and the largest scale), where exp's conditioning leaves the fp32 result
+    # within ~1e-6 of the float64 closed form
+    a = np.linspace(-0.25, 0.25, 24).astype(np.float32)
+    a[8:] = np.random.default_rng(60).permutation(a[8:])   # a non-symmetric logit pattern
+    a = orc.tf32_round(a)                                  # exact TF32 values
+    assert np.array_equal(brute64.round_tf32(a), a.astype(np.float64))
+    fn = np.zeros((24, K), np.float32)
+    fn[:, 0] = a
+    scale = np.array([0.25, 1.5, 3.0], np.float32)
+    base = np.random.default_rng(61).normal(0.0, 0.5, 24).astype(np.float32)
+    out = orc.boundary(orc.MODE_PRE_ONLY, res, fn, scale, base, None)
+    assert np.array_equal(out["mix"][0], a)
+    rstd = 1.0 / np.sqrt(1.0 / K + 1e-6)
+    v = a.astype(np.float64) * rstd
+    b = base.astype(np.float64)
+    pre = brute64.sigmoid(v[:4] * 0.25 + b[:4]) + 1e-6
+    post = 2.0 * brute64.sigmoid(v[4:8] * 1.5 + b[4:8])
+    comb = brute64.softmax_sinkhorn((v[8:] * 3.0 + b[8:]).reshape(4, 4), 20, 1e-6)
+    assert np.allclose(out["pre"][0], pre, rtol=2e-6, atol=0)
+    assert np.allclose(out["post"][0], post, rtol=2e-6, atol=0)
+    assert np.allclose(out["comb"][0], comb, rtol=1e-5, atol=1e-9)
+    # each group away from the others' scales: the check above discriminates
+    for wrong in (1.5, 3.0):
+        assert not np.allclose(brute64.sigmoid(v[:4] * wrong + b[:4]) + 1e-6, pre, rtol=1e-3)
+    for wrong in (0.25, 3.0):
+        assert not np.allclose(2.0 * brute64.sigmoid(v[4:8] * wrong + b[4:8]), post, rtol=1e-3)
+    for wrong in (0.25, 1.5):
+        alt = brute64.softmax_sinkhorn((v[8:] * wrong + b[8:]).reshape(4, 4), 20, 1e-6)
+        assert not np.allclose(alt, comb, rtol=1e-3)
+
+
+MODES_ALL = ("shifted", "unshifted", "pre")
+
+
+def _oracle_mode(mode, d, iters=20, norm_w=True):
+    kw = {}
+    if mode != "pre":
+        kw = dict(x=d["x"], post_mix=d["post"], comb=d["comb"])
+    if mode == "shifted":
+        kw["pre_lag"] = d["pre_lag"]
+    m = {"pre": orc.MODE_PRE_ONLY, "unshifted": orc.MODE_FUSED_UNSHIFTED,
+         "shifted": orc.MODE_FUSED_SHIFTED}[mode]
+    return orc.boundary(m, d["residual"], d["fn"], d["scale"], d["base"],
+                        d["norm_w"] if norm_w else None,
+                        params=orc.OracleParams(sinkhorn_iters=iters), **kw)
+
+
+def _ulps(a, b):
+    def ordered(u):
+        v = u.astype(np.int32)
+        return np.where(v & 0x8000, -(v & 0x7FFF), v)
+    return np.abs(ordered(a) - ordered(b))
+
+
+@pytest.mark.parametrize("scale", [(0.5, 0.5, 0.5), (0.25, 1.5, 3.0)])
+@pytest.mark.parametrize("mode", MODES_ALL)
+@pytest.mark.parametrize("norm_w", [True, False])
+def test_whole_op_matches_float64_brute_force_on_tiny_workload(mode, norm_w, scale):
+    """The whole boundary on the tiny workload (4 tokens, hidden 256, seed 0)
+    against the float64 brute force (same steps, double everywhere, bf16
+    rounding at the same points): the updated residual and the layer input
+    agree bit for bit on this workload (the fp32 chains' rounding never
+    moves a bf16 result here; the stress pin below bounds it in general),
+    the mixes within 1e-6 of max(|mix|, ||terms||_2), rstd within 1e-6
+    relative, and pre / post / comb within 1e-6 relative; with the
+    workload's equal scales and with distinct per-group scales."""
+    d = synth.workload_inputs("tiny_t4_h256", scale=scale)
+    o = _oracle_mode(mode, d, norm_w=norm_w)
+    b = brute64.boundary(mode, d, norm_w="f32" if norm_w else None)
+    if mode != "pre":
+        assert np.array_equal(o["residual_out"], b["residual_out"])
+    assert np.array_equal(o["layer_input"], b["layer_input"])
+    sc = np.maximum(np.abs(b["mix"]), b["mix_scale"])
+    assert np.all(np.abs(o["mix"] - b["mix"]) <= 1e-6 * sc)
+    assert np.allclose(o["rstd"], b["rstd"], rtol=1e-6, atol=0)
+    assert np.allclose(o["rstd_li"], b["rstd_li"], rtol=1e-6, atol=0)
+    for k in ("pre", "post", "comb"):
+        assert np.allclose(o[k], b[k], rtol=1e-6, atol=1e-9), k
+
+
+@pytest.mark.parametrize("iters", [1, 5, 20])
+def test_whole_op_stress_against_float64_with_the_chains_error_bound(iters):
+    """Stress inputs (residual ~ N(0, 8) with 1 % of entries x100, base ~
+    N(0, 4): sigmoid saturates, the update cancels). The updated residual
+    is the pages' fp32 flush-to-zero FMA chain rounded to bf16; against the
+    exact value rounded once, it may differ by the chain's own error: at
+    most 1 bf16 ulp plus 5 fp32 roundings of the chain's largest partial
+    magnitude (post*x + sum |comb*res|). Every element is within that, and
+    the layer input within 1 ulp; coefficients within 1e-5 relative + 1e-7,
+    mixes within 1e-6 of max(|mix|, ||terms||_2)."""
+    d = synth.make_inputs(16, 512, seed=4, residual_std=8.0, outlier_frac=0.01,
+                          outlier_mult=100.0, base_std=4.0)
+    for mode in MODES_ALL:
+        o = _oracle_mode(mode, d, iters=iters)
+        b = brute64.boundary(mode, d, iters=iters)
+        if mode != "pre":
+            res = brute64.from_bits(d["residual"])
+            x = brute64.from_bits(d["x"])
+            mag = (np.abs(d["post"].astype(np.float64))[:, :, None] * np.abs(x)[:, None, :]
+                   + np.einsum("tjs,tjh->tsh", np.abs(d["comb"].astype(np.float64)), np.abs(res)))
+            go, gb = brute64.from_bits(o["residual_out"]), brute64.from_bits(b["residual_out"])
+            ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(gb), 2.0 ** -126))[1] - 8)
+            bound = ulp + 5 * 2.0 ** -24 * mag
+            assert np.all(np.abs(go - gb) <= bound), mode
+        assert _ulps(o["layer_input"], b["layer_input"]).max() <= 1, mode
+        for k in ("pre", "post", "comb"):
+            assert np.all(np.abs(o[k] - b[k]) <= 1e-5 * np.abs(b[k]) + 1e-7), (mode, k)
+        sc = np.maximum(np.abs(b["mix"]), b["mix_scale"])
+        assert np.all(np.abs(o["mix"] - b["mix"]) <= 1e-6 * sc), mode
+
+
+def test_brute_force_rounding_helpers():
+    """The float64 reference's own roundings against library routines: bf16
+    against torch's RNE conversion (on float32 inputs, whose float64 value
+    is exact), TF32 against the arithmetic rounding above."""
+    rng = np.random.default_rng(62)
+    f = (rng.standard_normal(50_000) * np.exp(rng.uniform(-20, 20, 50_000))).astype(np.float32)
+    assert np.array_equal(brute64.bf16_bits(brute64.round_bf16(f.astype(np.float64))),
+                          torch_bf16(f))
+    w = f[:5000]
+    assert np.array_equal(brute64.round_tf32(w),
+                          np.array([tf32_arith(float(v)) for v in w], np.float64))

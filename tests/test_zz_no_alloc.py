@@ -61,6 +61,83 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(T, H, shifted):
             assert torch.equal(_bits(a), _bits(b)), f"call {call}"
 
 
+@pytest.mark.parametrize("scratch", ["noalloc", "shared_workspace"])
+def test_alternating_shapes_captured_and_eager_on_one_scratch(scratch):
+    """Calls of two shapes (8 and 16 tokens at hidden 7168) share one scratch
+    area: the library's fixed array, or one caller workspace sized for the
+    larger. Each shape is captured into a CUDA graph of its own; replays of
+    the two graphs are interleaved with eager calls of both shapes. A call's
+    flag value must never be one that another shape's flag words already
+    hold (a captured call takes its value from a cell at a fixed place of
+    the scratch, never covered by any shape's flags); every output is
+    compared bitwise with the workspace entry point on a private workspace."""
+    H = 7168
+    dev = "cuda"
+    shapes = (8, 16)
+    ws_shared = torch.empty(max(ops.workspace_bytes(T, H) for T in shapes), dtype=torch.uint8,
+                            device=dev)
+    case = {}
+    for T in shapes:
+        d = synth.make_inputs(T, H, seed=950 + T)
+        c = dict(x=B(d["x"]), res=B(d["residual"]), post=F(d["post"]), comb=F(d["comb"]),
+                 pl=F(d["pre_lag"]), w=ops.mhc_prepare_weight(F(d["fn"])), scale=F(d["scale"]),
+                 base=F(d["base"]), nw=F(d["norm_w"]))
+        c["ref"] = ops.mhc_boundary_fused(c["x"], c["res"], c["post"], c["comb"], c["w"],
+                                          c["scale"], c["base"], c["nw"], c["pl"])
+        c["outs"] = dict(residual_out=torch.empty_like(c["res"]),
+                         layer_input=torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+                         pre_out=torch.empty(T, 4, device=dev), post_out=torch.empty(T, 4, device=dev),
+                         comb_out=torch.empty(T, 4, 4, device=dev))
+        case[T] = c
+    torch.cuda.synchronize()
+
+    def call(T, stream=None):
+        c = case[T]
+        args = (c["x"], c["res"], c["post"], c["comb"], c["w"], c["scale"], c["base"], c["nw"],
+                c["pl"])
+        if scratch == "noalloc":
+            ops.mhc_boundary_fused_noalloc(*args, stream=stream, **c["outs"])
+        else:
+            ops.mhc_boundary_fused(*args, workspace=ws_shared, stream=stream, **c["outs"])
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graphs = {}
+    with torch.cuda.stream(s):
+        for T in shapes:
+            call(T, stream=s)                        # first call on the device, before capture
+        torch.cuda.synchronize()
+        for T in shapes:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                call(T, stream=s)
+            graphs[T] = g
+    torch.cuda.synchronize()
+
+    def check(T, what):
+        torch.cuda.synchronize()
+        assert ops.mhc_get_device_status() == 0, what
+        for a, b in zip([case[T]["outs"][k] for k in ("residual_out", "layer_input", "pre_out",
+                                                     "post_out", "comb_out")], case[T]["ref"]):
+            assert torch.equal(_bits(a), _bits(b)), what
+        for t in case[T]["outs"].values():
+            t.view(torch.uint8).fill_(0xEE)
+        torch.cuda.synchronize()
+
+    for T in shapes:
+        for t in case[T]["outs"].values():
+            t.view(torch.uint8).fill_(0xEE)
+    sequence = [("eager", 16), ("graph", 8), ("eager", 16), ("graph", 16), ("graph", 8),
+                ("eager", 8), ("graph", 16), ("graph", 16), ("eager", 16), ("graph", 8),
+                ("eager", 8), ("graph", 8), ("graph", 16)]
+    for i, (kind, T) in enumerate(sequence):
+        if kind == "eager":
+            call(T)
+        else:
+            graphs[T].replay()
+        check(T, f"step {i}: {kind} T={T}")
+
+
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     lib = ops.load()
     p = ops.Params().c()
