@@ -167,7 +167,11 @@ def _unshifted_li_excess(mode, d, g, o, li_gpu, norm, rows):
     r = _f64(stream)                                             # [t, 4, H]
     p_o = o["pre"].astype(np.float64)
     p_g = sel(g["pre"]).astype(np.float64)
-    E = np.einsum("tj,tjh->th", np.abs(p_g - p_o), np.abs(r))
+    # the two exact collapse sums are at most E apart; each side forms its
+    # own as a 4-step fp32 FMA chain (4 roundings, each at most 2^-24 of the
+    # chain's largest partial, itself at most sum_j |p_j r_j|)
+    mag = np.einsum("tj,tjh->th", np.abs(p_o), np.abs(r))
+    E = np.einsum("tj,tjh->th", np.abs(p_g - p_o), np.abs(r)) + 8 * 2.0 ** -24 * mag
     li_o = np.einsum("tj,tjh->th", p_o, r)
     if norm is None:
         scale = np.ones_like(li_o)
@@ -177,7 +181,7 @@ def _unshifted_li_excess(mode, d, g, o, li_gpu, norm, rows):
             w = _f64(orc.f32_to_bf16(d["norm_w"]))
         scale = o["rstd_li"].astype(np.float64)[:, None] * np.abs(w)[None, :]
     out_o = _f64(o["layer_input"])
-    bound = 2 * _ulp(out_o) + (E + _ulp(li_o)) * scale
+    bound = 2 * _ulp(out_o) + (E + _ulp(np.abs(li_o) + E)) * scale
     err = np.abs(_f64(li_gpu) - out_o)
     return float(np.max(err / bound)) if err.size else 0.0
 
@@ -195,10 +199,11 @@ def compare(mode: str, g: dict, o: dict, rows=None, li_ulps: int = 1, mixes: boo
     oracle's layer input computed from the GPU's own pre; at least 99.9 % of
     elements within 1 ulp of the independent oracle; and every element
     within a bound derived from the pre difference: with
-    E = sum_j |pre_gpu_j - pre_oracle_j| |r_j| (how far the two collapse
-    sums can be apart before rounding), |out_gpu - out_oracle| <=
-    2 ulp(out) + (E + ulp(li)) * rstd_li * |norm_w|, li = sum_j pre_j r_j
-    (the roundings of li and of the output on each side, and the sum's
+    E = sum_j |pre_gpu_j - pre_oracle_j| |r_j| + 8 * 2^-24 * sum_j |pre_j r_j|
+    (how far the two collapse sums can be apart: the pre difference, and
+    each side's 4-step fp32 FMA chain), |out_gpu - out_oracle| <=
+    2 ulp(out) + (E + ulp(|li| + E)) * rstd_li * |norm_w|, li = sum_j pre_j r_j
+    (the roundings of li and of the output on each side, and the sums'
     spread carried through the normalisation). The count of elements
     beyond 1 ulp and the largest distance are recorded in the stats."""
     sel = (lambda a: a) if rows is None else (lambda a: a[rows])
