@@ -317,6 +317,25 @@ mhc_status mhc_debug_coef_check(const float *values, const float *scale, const f
  * slice width. For tests and the benchmark's byte accounting. */
 mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width);
 
+/* Whether a shifted mhc_boundary_fused call of (T, H) on the current device
+ * runs on one thread-block cluster ("mhc_boundary" page, MhcBoundaryKernel:
+ * the hidden slices of one token tile in one cluster, exchanging partial
+ * mixes and sums of squares through distributed shared memory): *ctas = the
+ * cluster size (the number of hidden slices), or 0 when the call takes the
+ * slice-parallel streaming kernel. Cluster calls are the decode batches of
+ * 1 to 64 tokens whose H / 32 chunks split into at most 16 slices of at most
+ * 32 chunks, when params->batch_invariant is 0 and such a cluster can be
+ * resident on the device. They need no workspace contents (a workspace is
+ * still passed and checked); after the call its bytes 256 .. 256 + 112 T
+ * hold each token's 24 mixes and 4H sum of squares as 28 fp32 (the last
+ * three zero). Queries the device once per shape. */
+mhc_status mhc_plan_cluster(int64_t tokens, int hidden, int *ctas);
+
+/* Test and benchmark hook: path = 1 makes every later shifted call take the
+ * slice-parallel streaming kernel; 0 (the default) restores the cluster
+ * kernel for the calls mhc_plan_cluster describes. Process-wide. */
+void mhc_debug_set_decode_path(int path);
+
 #ifdef __cplusplus
 }
 #endif

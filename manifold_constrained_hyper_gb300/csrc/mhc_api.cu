@@ -270,6 +270,57 @@ bool encode_cached(int kind, CUtensorMap *m, const void *ptr, int H, long long T
     return ok;
 }
 
+// Decode path of the shifted form: 0 = a cluster where one fits, 1 = always
+// the slice-parallel streaming kernel (a test and benchmark hook).
+std::atomic<int> g_decode_path{0};
+
+// The shifted call of at most kClusterMaxTokens tokens on one thread-block
+// cluster: the largest cluster size C <= 16 dividing the H/32 chunks with at
+// most kClusterMaxChunks chunks per CTA; stages packed by token rows, as many
+// as fit beside the CTA's collapse buffer and the exchange areas (every chunk
+// resident when they all fit, else a ring of at least two). False when the
+// shape has no such plan.
+bool cluster_plan(long long T, int H, ClusterArgs *ca) {
+    if (T < 1 || T > kClusterMaxTokens) return false;
+    const int chunks = H / kChunk;
+    int C = 0;
+    for (int c = kClusterMaxCtas; c >= 1 && C == 0; --c)
+        if (chunks % c == 0 && chunks / c <= kClusterMaxChunks) C = c;
+    if (C == 0) return false;
+    const int nch = chunks / C;
+    const int R = static_cast<int>((T + 7) / 8 * 8);
+    const uint32_t stage = 5u * R * kRowBytes + kWBytes;          // a multiple of 512
+    const uint32_t li = static_cast<uint32_t>(nch) * R * kRowBytes;
+    const uint32_t owned_max = static_cast<uint32_t>((T + C - 1) / C);
+    const uint32_t part = (owned_max * C * kClusterRecFloats * 4 + 15u) & ~15u;
+    const uint32_t sql = (static_cast<uint32_t>(C * T) * 4 + 15u) & ~15u;
+    const uint32_t red = (16 * kPartVals + 32 + kClusterMaxTokens) * 4;
+    const uint32_t misc = 1024 /* alignment of li's end */ + 512 /* barriers */ +
+                          8 * 2 * kClusterMaxTokens * 4 + part + sql + red + 1024 /* base alignment */;
+    if (li + misc + 2 * stage > static_cast<uint32_t>(kClusterSmemMax) &&
+        li + misc + static_cast<uint32_t>(nch) * stage > static_cast<uint32_t>(kClusterSmemMax))
+        return false;
+    int NS = static_cast<int>((kClusterSmemMax - li - misc) / stage);
+    if (NS > nch) NS = nch;
+    if (NS > kClusterMaxStages) NS = kClusterMaxStages;
+    if (NS < 2 && NS < nch) return false;
+    ca->T = static_cast<int>(T);
+    ca->H = H;
+    ca->ctas = C;
+    ca->nch = nch;
+    ca->rows = R;
+    ca->stages = NS;
+    ca->stage_bytes = stage;
+    ca->li_off = NS * stage;
+    ca->bar_off = (ca->li_off + li + 1023u) & ~1023u;
+    ca->sums_off = ca->bar_off + 512;
+    ca->part_off = ca->sums_off + 8 * 2 * kClusterMaxTokens * 4;
+    ca->sql_off = ca->part_off + part;
+    ca->red_off = ca->sql_off + sql;
+    ca->smem_bytes = ca->red_off + red + 1024;
+    return ca->smem_bytes <= static_cast<uint32_t>(kClusterSmemMax);
+}
+
 mhc_status check_params(const mhc_params *p) {
     if (!p) return MHC_ERR_NULL;
     if (p->sinkhorn_iters < 1) return MHC_ERR_SHAPE;
@@ -333,6 +384,42 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     if (!get_encoder()) return MHC_ERR_CUDA;
 
     const bool invariant = params->batch_invariant != 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t *const ws8 = static_cast<uint8_t *>(workspace);
+    if (mode == FUSED_SHIFTED && !invariant && g_decode_path.load() == 0) {
+        // a decode batch on one thread-block cluster: one kernel, no flags
+        ClusterArgs ca;
+        if (cluster_plan(T, H, &ca) && cluster_fits(ca.ctas, ca.smem_bytes)) {
+            CUtensorMap m_res, m_x, m_rout;
+            if (!encode_cached(0, &m_res, residual, H, T) || !encode_cached(1, &m_x, x, H, T) ||
+                !encode_cached(0, &m_rout, residual_out, H, T))
+                return MHC_ERR_CUDA;
+            ca.post = post;
+            ca.comb = comb;
+            ca.pre_lag = pre_lag;
+            ca.weight = static_cast<const uint8_t *>(weight);
+            ca.status = dev->status;
+            ca.timeout_ns = g_timeout_ns.load();
+            ca.coef = coef_args(scale, base, params);
+            ca.norm_w = norm_w;
+            ca.nw_bf16 = norm_dtype == MHC_BF16;
+            ca.out32 = (reinterpret_cast<uintptr_t>(layer_input) & 31u) == 0;
+            ca.layer_input = layer_input;
+            ca.pre_out = pre_out;
+            ca.post_out = post_out;
+            ca.comb_out = comb_out;
+            // the reduced mixes, after the epoch cell (the workspace holds
+            // at least T x 128 bytes there for any plan)
+            ca.mix_out = reinterpret_cast<float *>(ws8 + kCellBytes);
+            if (mhc_status s = cuda_status(launch_cluster(m_res, m_x, m_rout, ca, st))) return s;
+            if (t_between_event) {
+                cudaEvent_t ev = t_between_event;
+                t_between_event = nullptr;
+                if (cudaEventRecord(ev, st) != cudaSuccess) return MHC_ERR_CUDA;
+            }
+            return MHC_OK;
+        }
+    }
     int S = 0, w = 0;
     if (invariant)
         plan_invariant(H, &S, &w);
@@ -345,13 +432,11 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
         if (!encode_cached(1, &m_x, x, H, T) || !encode_cached(0, &m_rout, residual_out, H, T))
             return MHC_ERR_CUDA;
     }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     StreamArgs sa;
     sa.post = post;
     sa.comb = comb;
     sa.pre_lag = pre_lag;
     sa.weight = static_cast<const uint8_t *>(weight);
-    uint8_t *const ws8 = static_cast<uint8_t *>(workspace);
     sa.partials = reinterpret_cast<float *>(ws8 + kCellBytes);
     sa.status = dev->status;
     sa.T = T;
@@ -575,6 +660,22 @@ mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual, const
                         residual_out, layer_input, pre_out, post_out, comb_out, workspace,
                         workspace_bytes, stream);
 }
+
+mhc_status mhc_plan_cluster(int64_t tokens, int hidden, int *ctas) {
+    if (!ctas) return MHC_ERR_NULL;
+    *ctas = 0;
+    if (tokens < 0) return MHC_ERR_SHAPE;
+    if (!hidden_ok(hidden)) return MHC_ERR_UNSUPPORTED;
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    ClusterArgs ca;
+    if (g_decode_path.load() == 0 && cluster_plan(tokens, hidden, &ca) &&
+        cluster_fits(ca.ctas, ca.smem_bytes))
+        *ctas = ca.ctas;
+    return MHC_OK;
+}
+
+void mhc_debug_set_decode_path(int path) { g_decode_path.store(path == 1 ? 1 : 0); }
 
 mhc_status mhc_get_device_status(void *stream) {
     DeviceInfo *dev = nullptr;

@@ -91,6 +91,50 @@ struct FinishArgs {
     int H;
 };
 
+// Decode calls on one thread-block cluster: at most this many tokens (one
+// tile, a quarter of the worker warps' lanes per token at most), at most
+// kClusterMaxCtas CTAs (hidden slices), each with at most kClusterMaxChunks
+// chunks of 32 and kClusterMaxStages pipeline stages.
+constexpr int kClusterMaxTokens = 64;
+constexpr int kClusterMaxCtas = 16;
+constexpr int kClusterMaxChunks = 32;
+constexpr int kClusterMaxStages = 16;
+constexpr int kClusterRecFloats = 28;               // a token's 25 values pushed to its owner, padded
+constexpr int kClusterSmemMax = 232448;             // dynamic shared memory per CTA (227 KB)
+
+// Arguments of the cluster kernel: one cluster of `ctas` CTAs, CTA r owning
+// hidden chunks r, r + ctas, ... (nch of them) of the one tile of T tokens.
+// Shared-memory offsets are from the 1024-byte-aligned base.
+struct ClusterArgs {
+    const float *post;       // [T,4]
+    const float *comb;       // [T,4,4]
+    const float *pre_lag;    // [T,4]
+    const uint8_t *weight;   // prepared tiles
+    unsigned int *status;    // device status word
+    unsigned long long timeout_ns;
+    int T, H;
+    int ctas;                // cluster size = hidden slices
+    int nch;                 // chunks per CTA
+    int rows;                // token rows per box (T rounded up to 8)
+    int stages;              // pipeline stages (== nch when every chunk stays resident)
+    uint32_t stage_bytes;    // 4 residual boxes + the x box + a 12 KB weight tile
+    uint32_t li_off;         // the CTA's collapse [nch][rows][32] bf16 (unswizzled)
+    uint32_t bar_off;        // mbarriers and the TMEM slot / abort flag
+    uint32_t sums_off;       // worker warps' per-token sums [8][2][64] fp32
+    uint32_t part_off;       // owned tokens' pushed values [owned][ctas][kClusterRecFloats]
+    uint32_t sql_off;        // every CTA's collapse sums of squares [ctas][T] fp32
+    uint32_t red_off;        // coefficient reduction [16][25], constants [32], rstd_li [64]
+    uint32_t smem_bytes;     // dynamic shared memory of the launch
+    CoefArgs coef;
+    const void *norm_w;      // [H] or NULL
+    int nw_bf16;
+    int out32;               // layer_input 32-byte aligned
+    uint16_t *layer_input;   // [T,H]
+    float *pre_out, *post_out, *comb_out;
+    float *mix_out;          // [T][kClusterRecFloats]: each token's reduced 24 mixes and
+                             // 4H sum of squares, kept in the caller's scratch (or NULL)
+};
+
 constexpr int kGridCap = 152;                       // persistent CTAs: one per GB300 SM
 constexpr int kStreamStages = 4;                    // pipeline stages of the streaming kernel
 constexpr int kDecodeMaxTokens = 64;                // most tokens of the decode worker mapping
@@ -103,6 +147,13 @@ size_t stream_smem_bytes();
 cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x,
                           const CUtensorMap &rout, const StreamArgs &a, int n_slices, int n_items,
                           int grid, cudaStream_t s);
+// Shifted decode call on one thread-block cluster of a.ctas CTAs (the hidden
+// slices exchange their partials through distributed shared memory).
+cudaError_t launch_cluster(const CUtensorMap &res, const CUtensorMap &x, const CUtensorMap &rout,
+                           const ClusterArgs &a, cudaStream_t s);
+// Whether a cluster of `ctas` CTAs with `smem` bytes of dynamic shared memory
+// can be resident on the current device (checked once per size and device).
+bool cluster_fits(int ctas, uint32_t smem);
 cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,

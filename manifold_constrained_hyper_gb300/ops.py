@@ -27,7 +27,8 @@ EXPORTS = ("mhc_weight_bytes", "mhc_prepare_weight", "mhc_post", "mhc_workspace_
            "mhc_pre", "mhc_boundary_fused", "mhc_get_device_status", "mhc_last_timeout_site",
            "mhc_status_string", "mhc_set_wait_timeout_ns", "mhc_debug_unarmed_wait",
            "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc",
-           "mhc_debug_rcp_check", "mhc_pre_split_k", "mhc_debug_coef_check")
+           "mhc_debug_rcp_check", "mhc_pre_split_k", "mhc_debug_coef_check", "mhc_plan_cluster",
+           "mhc_debug_set_decode_path")
 
 
 class MhcError(RuntimeError):
@@ -94,6 +95,8 @@ def load():
         "mhc_debug_coef_check": (i32, [P, P, P, PP, i32, i64, P, P, P]),
         "mhc_pre_split_k": (i32, [P, P, P, i32, P, P, P, i32, PP, i64, i32, P, P, P, P, P]),
         "mhc_plan": (i32, [i64, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+        "mhc_plan_cluster": (i32, [i64, i32, ctypes.POINTER(ctypes.c_int)]),
+        "mhc_debug_set_decode_path": (None, [i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -165,6 +168,20 @@ def plan(tokens: int, hidden: int):
     s, w = ctypes.c_int(), ctypes.c_int()
     _check(load().mhc_plan(tokens, hidden, ctypes.byref(s), ctypes.byref(w)), "mhc_plan")
     return s.value, w.value
+
+
+def plan_cluster(tokens: int, hidden: int) -> int:
+    """Cluster size of a shifted call of (tokens, hidden) on the current
+    device, or 0 when it takes the slice-parallel streaming kernel."""
+    c = ctypes.c_int()
+    _check(load().mhc_plan_cluster(tokens, hidden, ctypes.byref(c)), "mhc_plan_cluster")
+    return c.value
+
+
+def mhc_debug_set_decode_path(path: int):
+    """1: every later shifted call takes the slice-parallel streaming kernel;
+    0: the cluster kernel where it applies (the default)."""
+    load().mhc_debug_set_decode_path(int(path))
 
 
 def mhc_prepare_weight(fn: torch.Tensor, out: torch.Tensor | None = None, stream=None):

@@ -75,6 +75,13 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
         out["residual_out_dev"] = ro
     torch.cuda.synchronize()
     assert ops.mhc_get_device_status() == 0
+    if mode == "shifted" and not (params and params.batch_invariant) and ops.plan_cluster(T, H):
+        # a cluster call keeps each token's reduced values (24 mixes, the 4H
+        # sum of squares, padding) at bytes 256 .. 256 + 112 T: one "slice"
+        part = ws[256: 256 + T * 112].view(torch.float32).view(1, T, 28)[..., :25]
+        out.update(layer_input_dev=li, pre=pr.cpu().numpy(), post=po.cpu().numpy(),
+                   comb=cb.cpu().numpy(), partials=part.cpu().numpy(), path="cluster")
+        return out
     S, _ = ops.plan(T, H)
     # the library's internal partials, 25 values per token and slice (24
     # mixes, then the 4H sum of squares), in a block of 128 x 32 floats per
@@ -98,7 +105,7 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
         blk = raw[..., : 25 * 128].reshape(tiles, S, 25, 128).permute(1, 0, 3, 2)
     part = blk.reshape(S, tiles * 128, 25)[:, :T, :].cpu().numpy()
     out.update(layer_input_dev=li, pre=pr.cpu().numpy(), post=po.cpu().numpy(),
-               comb=cb.cpu().numpy(), partials=part)
+               comb=cb.cpu().numpy(), partials=part, path="slices")
     return out
 
 
