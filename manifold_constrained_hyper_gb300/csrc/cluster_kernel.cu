@@ -13,7 +13,8 @@
 // into per-token sums and writes the lagged collapse into a buffer of the CTA
 // that outlives the stages; the producer TMA-stores the updated residual; one
 // thread issues 8 tcgen05 MMAs (M = 128 rows, of which the first T are
-// tokens, N = 48 hi/lo weight rows) into one TMEM accumulator. The stages are
+// tokens, N = 48 hi/lo weight rows) into a TMEM accumulator (four, taken in
+// turn by the chunks, added at the end). The stages are
 // packed by token rows (4 residual boxes, the x box, the weight tile), so at
 // up to 8 tokens every chunk of a 14-chunk slice is resident at once and the
 // producer sends every load during the set-up.
@@ -52,7 +53,13 @@ constexpr int kWorkThreads = 256;
 constexpr int kFinThreads = 128;
 constexpr int kFinBarrier = 1;
 constexpr int kWorkBarrier = 2;
+// The CTA's chunks rotate over kAccs TMEM accumulators (kAccCols columns
+// each, 48 used), so that no fp32 accumulation chain is longer than 8 chunks
+// (1024 products, as in the streaming kernel's largest item); the finishers
+// add the accumulators in a fixed order.
+constexpr int kAccs = 4;
 constexpr int kAccCols = 64;
+constexpr uint32_t kTmemCols = kAccs * kAccCols;
 constexpr int kRegsProducer = 40, kRegsWorker = 184, kRegsFinisher = 96;
 static_assert(128 * (kRegsProducer + kRegsFinisher) + 256 * kRegsWorker <= kThreads * 128,
               "register split exceeds the CTA's allocation (512 threads x 128 at launch)");
@@ -209,7 +216,7 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
     if (tid < 27) stage_coef_consts(a.coef, consts, tid);
     __syncwarp();
     if (warp == 0) {
-        tmem_alloc(smem_addr(tmem_slot), kAccCols);
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
     // worker lanes: the token they update and its coefficients (loaded now,
@@ -294,7 +301,8 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
                         const uint64_t ad = smem_desc_sw64(sb + s * R * kRowBytes + kk * 32, 8 * kRowBytes);
                         const uint64_t bd = smem_desc_sw64(
                             sb + res_bytes + x_bytes + s * kWRows * kRowBytes + kk * 32, 8 * kRowBytes);
-                        tc_mma_bf16(tmem_base, ad, bd, kIdesc, (g | s | kk) != 0);
+                        tc_mma_bf16(tmem_base + (g % kAccs) * kAccCols, ad, bd, kIdesc,
+                                    (g >= kAccs) | s | kk);
                     }
                 }
                 tc_commit(mma_done(st));
@@ -313,7 +321,7 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
             int local = 0;
             mbar_wait(exit_bar, 0, &local, tmo, a.status, SITE_C_DRAIN);
             tc_fence_after();
-            tmem_dealloc(tmem_base, kAccCols);
+            tmem_dealloc(tmem_base, kTmemCols);
         }
     } else if (warp < 12) {
         // ---------------------------------------------------- elementwise workers
@@ -431,12 +439,23 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
                 ssql += sums[(w2 * 2 + 1) * kClusterMaxTokens + t];
             }
         }
+        // the accumulators in use (min(nch, kAccs)), added as ((a0 + a1) + a2) + a3
+        const int nacc = nch < kAccs ? nch : kAccs;
         uint32_t v[48];
         const uint32_t acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-        tmem_ld16(acc + 0, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-        tmem_ld16(acc + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-        tmem_ld16(acc + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
-        tmem_ld_wait();
+#pragma unroll
+        for (int b = 0; b < 3; ++b) {
+            uint32_t w[16];
+            tmem_ld16(acc + 16 * b, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * b]));
+            tmem_ld_wait();
+            for (int k = 1; k < nacc; ++k) {
+                tmem_ld16(acc + k * kAccCols + 16 * b, w);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[16 * b + i] = __float_as_uint(__uint_as_float(v[16 * b + i]) + __uint_as_float(w[i]));
+            }
+        }
         tc_fence_before();
         ok = __all_sync(0xffffffffu, ok);
         if (ok && t < T) {
