@@ -322,18 +322,22 @@ mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width)
  * the hidden slices of one token tile in one cluster, exchanging partial
  * mixes and sums of squares through distributed shared memory): *ctas = the
  * cluster size (the number of hidden slices), or 0 when the call takes the
- * slice-parallel streaming kernel. Cluster calls are the decode batches of
- * 1 to 64 tokens whose H / 32 chunks split into at most 16 slices of at most
- * 32 chunks, when params->batch_invariant is 0 and such a cluster can be
- * resident on the device. They need no workspace contents (a workspace is
+ * slice-parallel streaming kernel. A call can take a cluster when it has 1 to
+ * 64 tokens, params->batch_invariant is 0, its H / 32 chunks split into at
+ * most 16 slices of at most 32 chunks and such a cluster can be resident on
+ * the device; by default it does so where that is the faster path (a slice
+ * of one chunk, or of two chunks for up to 16 tokens: hidden sizes up to
+ * 1024; at hidden 7168 the slice-parallel kernel, which spreads the work over
+ * 112 CTAs instead of 16, is faster). Cluster calls need no workspace contents (a workspace is
  * still passed and checked); after the call its bytes 256 .. 256 + 112 T
  * hold each token's 24 mixes and 4H sum of squares as 28 fp32 (the last
  * three zero). Queries the device once per shape. */
 mhc_status mhc_plan_cluster(int64_t tokens, int hidden, int *ctas);
 
-/* Test and benchmark hook: path = 1 makes every later shifted call take the
- * slice-parallel streaming kernel; 0 (the default) restores the cluster
- * kernel for the calls mhc_plan_cluster describes. Process-wide. */
+/* Test and benchmark hook for the shifted form's decode path, process-wide:
+ * 0 (the default) as described at mhc_plan_cluster; 1 every later call takes
+ * the slice-parallel streaming kernel; 2 every call that can take a cluster
+ * does. Other values act as 0. */
 void mhc_debug_set_decode_path(int path);
 
 #ifdef __cplusplus

@@ -6,15 +6,15 @@
 // summed in rank order). No workspace, no global flags: one kernel per call.
 //
 // CTA r of a cluster of C owns hidden chunks r, r + C, r + 2C, ... (nch chunks
-// of 32). Per chunk, as in the streaming kernel: TMA-load the four residual
-// boxes and the x box (rows = T rounded up to 8, one box per stream) and
+// of 32). Per chunk, as in the streaming kernel: TMA-load the residual box
+// [4 streams][rows][32] and the x box (rows = T rounded up to 8) and
 // bulk-load the chunk's 12 KB prepared weight tile; a worker warp updates the
 // residual in shared memory (the flush-to-zero FMA chain), folds the squares
 // into per-token sums and writes the lagged collapse into a buffer of the CTA
-// that outlives the stages; the producer TMA-stores the updated residual; one
-// thread issues 8 tcgen05 MMAs (M = 128 rows, of which the first T are
-// tokens, N = 48 hi/lo weight rows) into a TMEM accumulator (four, taken in
-// turn by the chunks, added at the end). The stages are
+// that outlives the stages; the producer TMA-stores the updated residual;
+// four threads (one per stream, in four warps) issue the chunk's 8 tcgen05
+// MMAs (M = 128 rows, of which the first T are tokens, N = 48 hi/lo weight
+// rows) into four TMEM accumulators, one per stream, added at the end. The stages are
 // packed by token rows (4 residual boxes, the x box, the weight tile), so at
 // up to 8 tokens every chunk of a 14-chunk slice is resident at once and the
 // producer sends every load during the set-up.
@@ -29,11 +29,11 @@
 // same order everywhere, so the same rstd_li) and writes its slice of the
 // layer input. All reductions run in a fixed order: results are deterministic.
 //
-// Warps: 0 TMA producer and TMEM owner, 1 MMA issuer, 2-3 idle, 4-11 workers
+// Warps: 0 TMA producer and TMEM owner, 1-3 idle, 4-11 workers
 // (worker warp w takes the chunks of stages w, w + 8, ... or, above 32
 // tokens, token half w % 2 of the chunks of stages w / 2, w / 2 + 4, ...),
-// 12-15 finishers (token 32 (warp % 4) + lane, the TMEM lane quarter of the
-// warp). Every wait on a barrier is
+// 12-15 MMA issuers (stream warp % 4), then finishers (token 32 (warp % 4) +
+// lane, the TMEM lane quarter of the warp). Every wait on a barrier is
 // bounded; the two cluster barriers (after barrier initialisation, and before
 // exit so that no CTA leaves while a peer may still write into its shared
 // memory) are reached by every thread without any wait before them that is
@@ -53,11 +53,12 @@ constexpr int kWorkThreads = 256;
 constexpr int kFinThreads = 128;
 constexpr int kFinBarrier = 1;
 constexpr int kWorkBarrier = 2;
-// The CTA's chunks rotate over kAccs TMEM accumulators (kAccCols columns
-// each, 48 used), so that no fp32 accumulation chain is longer than 8 chunks
-// (1024 products, as in the streaming kernel's largest item); the finishers
-// add the accumulators in a fixed order.
+// One TMEM accumulator per residual stream (kAccCols columns each, 48 used),
+// each fed by its own issuing warp (two MMAs per chunk); no fp32 accumulation
+// chain is longer than 2 MMAs per chunk (1024 products at the most chunks);
+// the finishers add the four in a fixed order.
 constexpr int kAccs = 4;
+constexpr int kEarlyLoads = 2;          // chunks whose loads go out during the set-up
 constexpr int kAccCols = 64;
 constexpr uint32_t kTmemCols = kAccs * kAccCols;
 constexpr int kRegsProducer = 40, kRegsWorker = 184, kRegsFinisher = 96;
@@ -181,9 +182,8 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
         const uint32_t sb = base + st * SB;
         const int hc = hidden_of(g);
         mbar_arrive_expect_tx(full(st), load_bytes);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-            tma_load_3d(sb + s * R * kRowBytes, &tm_res, hc, 0, s, full(st), pol_load);
+        // one box of [4 streams][R rows][32] lands as the four packed boxes
+        tma_load_3d(sb, &tm_res, hc, 0, 0, full(st), pol_load);
         tma_load_2d(sb + res_bytes, &tm_x, hc, 0, full(st), pol_load);
         bulk_load(sb + res_bytes + x_bytes, a.weight + static_cast<size_t>(hc / kChunk) * kWBytes,
                   kWBytes, full(st), pol_keep);
@@ -199,9 +199,9 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
         for (int i = 0; i < NS; ++i) {
             mbar_init(full(i), 1);
             mbar_init(ready(i), T > 32 ? 2 : 1);    // the worker warps of the chunk
-            mbar_init(mma_done(i), 1);
+            mbar_init(mma_done(i), kAccs);           // one commit per issuing warp
         }
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, kAccs);
         mbar_init(sums_full, 8);
         mbar_init(part_bar, 1);
         mbar_init(sql_bar, 1);
@@ -211,7 +211,10 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
         // expected before any peer can push (the cluster barrier below)
         mbar_arrive_expect_tx(part_bar, static_cast<uint32_t>(n_own * C * kClusterRecFloats * 4));
         mbar_arrive_expect_tx(sql_bar, static_cast<uint32_t>(C * T * 4));
-        for (int g = 0; g < nch && g < NS; ++g) issue_load(g);
+        // the first two chunks' loads now; the producer sends the others
+        // once the set-up is done (one thread issuing every copy held the
+        // whole CTA's set-up back by ~2.5 us at 14 chunks)
+        for (int g = 0; g < nch && g < kEarlyLoads; ++g) issue_load(g);
     }
     if (tid < 27) stage_coef_consts(a.coef, consts, tid);
     __syncwarp();
@@ -251,16 +254,16 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------ TMA producer
             const uint64_t pol_out = policy_evict_first();
-            int loaded = nch < NS ? nch : NS;
+            const int first = nch < NS ? nch : NS;
+            for (int g0 = kEarlyLoads; g0 < first; ++g0) issue_load(g0);
+            int loaded = first;
             int g = 0;
             for (; g < nch; ++g) {
                 const int st = g % NS;
                 if (!mbar_wait(ready(st), (g / NS) & 1, abort_flag, tmo, a.status, SITE_C_PROD_READY))
                     break;
                 const uint32_t sb = base + st * SB;
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    tma_store_3d(&tm_rout, hidden_of(g), 0, s, sb + s * R * kRowBytes, pol_out);
+                tma_store_3d(&tm_rout, hidden_of(g), 0, 0, sb, pol_out);
                 bulk_commit();
                 // refill the stage of the previous chunk once its store has
                 // read shared memory and its MMAs are done
@@ -280,40 +283,6 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
                     int local = 0;
                     mbar_wait(full(c % NS), (c / NS) & 1, &local, tmo, a.status, SITE_C_DRAIN);
                 }
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
-            int issued = 0;
-            for (int g = 0; g < nch; ++g) {
-                const int st = g % NS;
-                const uint32_t ph = (g / NS) & 1;
-                if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_C_MMA)) break;
-                if (!mbar_wait(ready(st), ph, abort_flag, tmo, a.status, SITE_C_MMA)) break;
-                tc_fence_after();
-                const uint32_t sb = base + st * SB;
-#pragma unroll
-                for (int s = 0; s < 4; ++s) {
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        // A: 128 rows from stream s's box (rows past T are
-                        // other data of the stage: their accumulator rows
-                        // are never read); B: the stream's 48 weight rows
-                        const uint64_t ad = smem_desc_sw64(sb + s * R * kRowBytes + kk * 32, 8 * kRowBytes);
-                        const uint64_t bd = smem_desc_sw64(
-                            sb + res_bytes + x_bytes + s * kWRows * kRowBytes + kk * 32, 8 * kRowBytes);
-                        tc_mma_bf16(tmem_base + (g % kAccs) * kAccCols, ad, bd, kIdesc,
-                                    (g >= kAccs) | s | kk);
-                    }
-                }
-                tc_commit(mma_done(st));
-                if (g == nch - 1) tc_commit(acc_full);
-                issued = g + 1;
-            }
-            if (issued > 0 && issued < nch) {
-                int local = 0;
-                const int c = issued - 1;
-                mbar_wait(mma_done(c % NS), (c / NS) & 1, &local, tmo, a.status, SITE_C_DRAIN);
-            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(exit_bar);
@@ -429,6 +398,42 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
         const int q = warp & 3;
         const int t = q * 32 + lane;
         const int ft = tid - 12 * 32;                  // 0..127 among the finishers
+        // ---- MMA issue: lane 0 of finisher warp q issues stream q's two
+        // MMAs of every chunk into accumulator q. One thread issues a
+        // tcgen05.mma about every 80 ns whatever its shape, while several
+        // warps issue concurrently, so the four streams go out in parallel.
+        if (lane == 0) {
+            constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
+            const uint32_t dcol = tmem_base + q * kAccCols;
+            int issued = 0;
+            for (int g = 0; g < nch; ++g) {
+                const int st = g % NS;
+                const uint32_t ph = (g / NS) & 1;
+                if (!mbar_wait(full(st), ph, abort_flag, tmo, a.status, SITE_C_MMA)) break;
+                if (!mbar_wait(ready(st), ph, abort_flag, tmo, a.status, SITE_C_MMA)) break;
+                tc_fence_after();
+                const uint32_t sb = base + st * SB;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    // A: 128 rows from stream q's box (rows past T are other
+                    // data of the stage: their accumulator rows are never
+                    // read); B: the stream's 48 weight rows
+                    const uint64_t ad = smem_desc_sw64(sb + q * R * kRowBytes + kk * 32, 8 * kRowBytes);
+                    const uint64_t bd = smem_desc_sw64(
+                        sb + res_bytes + x_bytes + q * kWRows * kRowBytes + kk * 32, 8 * kRowBytes);
+                    tc_mma_bf16(dcol, ad, bd, kIdesc, g | kk);
+                }
+                tc_commit(mma_done(st));
+                if (g == nch - 1) tc_commit(acc_full);
+                issued = g + 1;
+            }
+            if (issued > 0 && issued < nch) {
+                int local = 0;
+                const int c = issued - 1;
+                mbar_wait(mma_done(c % NS), (c / NS) & 1, &local, tmo, a.status, SITE_C_DRAIN);
+            }
+        }
+        __syncwarp();
         bool ok = mbar_wait(sums_full, 0, abort_flag, tmo, a.status, SITE_C_FIN);
         ok = mbar_wait(acc_full, 0, abort_flag, tmo, a.status, SITE_C_FIN) && ok;
         tc_fence_after();
@@ -439,8 +444,8 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
                 ssql += sums[(w2 * 2 + 1) * kClusterMaxTokens + t];
             }
         }
-        // the accumulators in use (min(nch, kAccs)), added as ((a0 + a1) + a2) + a3
-        const int nacc = nch < kAccs ? nch : kAccs;
+        // the four streams' accumulators, added as ((a0 + a1) + a2) + a3
+        constexpr int nacc = kAccs;
         uint32_t v[48];
         const uint32_t acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll
@@ -448,6 +453,7 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
             uint32_t w[16];
             tmem_ld16(acc + 16 * b, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * b]));
             tmem_ld_wait();
+#pragma unroll
             for (int k = 1; k < nacc; ++k) {
                 tmem_ld16(acc + k * kAccCols + 16 * b, w);
                 tmem_ld_wait();

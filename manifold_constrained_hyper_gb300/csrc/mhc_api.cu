@@ -224,11 +224,12 @@ bool encode_2d(CUtensorMap *m, const void *ptr, int H, long long T) {
 // bf16 [T, 4, H] viewed as (hidden, token, stream) so that a box lands in
 // shared memory as [stream][token][32 hidden] (one stream per box when the
 // call is a single tile).
-bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T) {
+bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T, bool all_streams = false) {
     const int br = box_rows_for(T);
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T), 4};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * 8, static_cast<cuuint64_t>(H) * 2};
-    cuuint32_t box[3] = {kChunk, static_cast<cuuint32_t>(br ? br : kTileT), br ? 1u : 4u};
+    cuuint32_t box[3] = {kChunk, static_cast<cuuint32_t>(br ? br : kTileT),
+                         br && !all_streams ? 1u : 4u};
     cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -237,7 +238,8 @@ bool encode_res(CUtensorMap *m, const void *ptr, int H, long long T) {
 }
 
 // Tensor maps of the last few calls of this host thread, by (kind, pointer,
-// H, T) (kind 0 residual-shaped, 1 x-shaped): a decode loop reuses its
+// H, T) (kind 0 residual-shaped, 1 x-shaped, 2 residual-shaped with the four
+// streams in one box of a call's token rows): a decode loop reuses its
 // buffers, and encoding costs host time.
 struct MapCache {
     struct Entry {
@@ -257,7 +259,7 @@ bool encode_cached(int kind, CUtensorMap *m, const void *ptr, int H, long long T
             return true;
         }
     }
-    const bool ok = kind == 0 ? encode_res(m, ptr, H, T) : encode_2d(m, ptr, H, T);
+    const bool ok = kind == 1 ? encode_2d(m, ptr, H, T) : encode_res(m, ptr, H, T, kind == 2);
     if (ok) {
         auto &x = t_maps.e[t_maps.next];
         t_maps.next = (t_maps.next + 1) % 8;
@@ -270,9 +272,20 @@ bool encode_cached(int kind, CUtensorMap *m, const void *ptr, int H, long long T
     return ok;
 }
 
-// Decode path of the shifted form: 0 = a cluster where one fits, 1 = always
-// the slice-parallel streaming kernel (a test and benchmark hook).
+// Decode path of the shifted form: 0 = a cluster where one fits and is the
+// faster, 1 = always the slice-parallel streaming kernel, 2 = a cluster
+// wherever one fits (test and benchmark hooks).
 std::atomic<int> g_decode_path{0};
+
+// Where the cluster kernel is the faster (measured, graph replay at 1 to 64
+// tokens and hidden 256 to 7168 against the slice-parallel streaming kernel):
+// when each CTA streams one chunk (by 1.4-4.3 us), or two chunks for up to 16
+// tokens (by ~0.8 us). With more chunks per CTA its 16 CTAs carry 4-14 times
+// the per-SM work of the slice-parallel kernel (weight tiles pulled from L2,
+// elementwise chains, MMA instructions) and lose.
+bool cluster_preferred(long long T, const ClusterArgs &ca) {
+    return ca.nch == 1 || (ca.nch == 2 && T <= 16);
+}
 
 // The shifted call of at most kClusterMaxTokens tokens on one thread-block
 // cluster: the largest cluster size C <= 16 dividing the H/32 chunks with at
@@ -386,13 +399,15 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     const bool invariant = params->batch_invariant != 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t *const ws8 = static_cast<uint8_t *>(workspace);
-    if (mode == FUSED_SHIFTED && !invariant && g_decode_path.load() == 0) {
+    const int path = g_decode_path.load();
+    if (mode == FUSED_SHIFTED && !invariant && path != 1) {
         // a decode batch on one thread-block cluster: one kernel, no flags
         ClusterArgs ca;
-        if (cluster_plan(T, H, &ca) && cluster_fits(ca.ctas, ca.smem_bytes)) {
+        if (cluster_plan(T, H, &ca) && (path == 2 || cluster_preferred(T, ca)) &&
+            cluster_fits(ca.ctas, ca.smem_bytes)) {
             CUtensorMap m_res, m_x, m_rout;
-            if (!encode_cached(0, &m_res, residual, H, T) || !encode_cached(1, &m_x, x, H, T) ||
-                !encode_cached(0, &m_rout, residual_out, H, T))
+            if (!encode_cached(2, &m_res, residual, H, T) || !encode_cached(1, &m_x, x, H, T) ||
+                !encode_cached(2, &m_rout, residual_out, H, T))
                 return MHC_ERR_CUDA;
             ca.post = post;
             ca.comb = comb;
@@ -669,13 +684,14 @@ mhc_status mhc_plan_cluster(int64_t tokens, int hidden, int *ctas) {
     DeviceInfo *dev = nullptr;
     if (mhc_status s = current_device(&dev)) return s;
     ClusterArgs ca;
-    if (g_decode_path.load() == 0 && cluster_plan(tokens, hidden, &ca) &&
-        cluster_fits(ca.ctas, ca.smem_bytes))
+    const int path = g_decode_path.load();
+    if (path != 1 && cluster_plan(tokens, hidden, &ca) &&
+        (path == 2 || cluster_preferred(tokens, ca)) && cluster_fits(ca.ctas, ca.smem_bytes))
         *ctas = ca.ctas;
     return MHC_OK;
 }
 
-void mhc_debug_set_decode_path(int path) { g_decode_path.store(path == 1 ? 1 : 0); }
+void mhc_debug_set_decode_path(int path) { g_decode_path.store(path == 1 || path == 2 ? path : 0); }
 
 mhc_status mhc_get_device_status(void *stream) {
     DeviceInfo *dev = nullptr;

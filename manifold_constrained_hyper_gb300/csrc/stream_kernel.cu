@@ -217,10 +217,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         for (int i = 0; i < kStages; ++i) {
             mbar_init(full(i), 1);
             mbar_init(ready(i), 8);
-            mbar_init(mma_done(i), 1);
+            mbar_init(mma_done(i), kDecodeMap ? 4 : 1);   // decode: one commit per stream's issuer
         }
         for (int b = 0; b < kAccBufs; ++b) {
-            mbar_init(acc_full(b), 1);
+            mbar_init(acc_full(b), kDecodeMap ? 4 : 1);
             mbar_init(acc_empty(b), 4);
             mbar_init(sums_full(b), 8);
             mbar_init(sums_empty(b), 4);
@@ -242,7 +242,8 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         if (kShifted)
             for (int g = 0; g < total && g < kStages; ++g) issue_load(g);
     }
-    constexpr uint32_t kTmemCols = kShifted && !kDecodeMap ? 512 : kAccBufs * kAccCols;
+    // decode variants: one accumulator per residual stream (4 x kAccCols)
+    constexpr uint32_t kTmemCols = kShifted && !kDecodeMap ? 512 : (kDecodeMap ? 4 : kAccBufs) * kAccCols;
     static_assert(kAccBufs * kAccCols + kLiBufs * kLiCols <= 512, "TMEM columns");
     if (warp == 0) {
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -323,7 +324,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             }
             // the stage buffers are free of this CTA's copies
             if (kShifted && a.coef_end) mbar_arrive(stages_free);
-        } else if (warp == 1 && lane == 0) {
+        } else if (warp == 1 && lane == 0 && !kDecodeMap) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
             int issued = 0;
@@ -760,6 +761,35 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // ---------------------------------------------------- finishers
         regs_dec_finisher();
         const int q = warp & 3;
+        if (kDecodeMap && lane == 0) {
+            // ---- decode variants: lane 0 of finisher warp q issues stream q's
+            // two MMAs of every chunk of the item into accumulator q (one
+            // thread issues a tcgen05.mma about every 80 ns whatever its
+            // shape, and several warps issue concurrently: the four streams
+            // go out in parallel instead of one after another)
+            constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
+            const uint32_t dcol = tmem_base + q * kAccCols;
+            int issued = 0;
+            for (int g = 0; g < total; ++g) {
+                if (!mbar_wait(full(g), 0, abort_flag, tmo, a.status, SITE_MMA_FULL)) break;
+                if (!mbar_wait(ready(g), 0, abort_flag, tmo, a.status, SITE_MMA_READY)) break;
+                tc_fence_after();
+                const uint32_t sb = base + g * kStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint64_t ad = smem_desc_sw64(sb + q * kTileT * kRowBytes + kk * 32, 8 * kRowBytes);
+                    const uint64_t bd = smem_desc_sw64(
+                        sb + kResBytes + kXBytes + q * kWRows * kRowBytes + kk * 32, 8 * kRowBytes);
+                    tc_mma_bf16(dcol, ad, bd, kIdesc, g | kk);
+                }
+                tc_commit(mma_done(g));
+                if (g == total - 1) tc_commit(acc_full(0));
+                issued = g + 1;
+            }
+            if (issued > 0 && issued < total)
+                drain_wait(mma_done(issued - 1), 0, tmo, a.status);
+        }
+        __syncwarp();
         // this call's flag value: from the host, or (a call captured into a
         // CUDA graph) one more than the workspace cell's, which the call then
         // advances itself. One thread reads the cell and hands the value to
@@ -826,6 +856,22 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 tmem_ld16(acc + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                 tmem_ld16(acc + 32, *reinterpret_cast<uint32_t(*)[16]>(&v[32]));
                 tmem_ld_wait();
+                if (kDecodeMap) {
+                    // the four streams' accumulators, added as ((a0 + a1) + a2) + a3
+#pragma unroll
+                    for (int s2 = 1; s2 < 4; ++s2) {
+#pragma unroll
+                        for (int blk = 0; blk < 3; ++blk) {
+                            uint32_t w[16];
+                            tmem_ld16(acc + s2 * kAccCols + 16 * blk, w);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                v[16 * blk + i] =
+                                    __float_as_uint(__uint_as_float(v[16 * blk + i]) + __uint_as_float(w[i]));
+                        }
+                    }
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {

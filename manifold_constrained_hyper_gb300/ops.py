@@ -179,8 +179,9 @@ def plan_cluster(tokens: int, hidden: int) -> int:
 
 
 def mhc_debug_set_decode_path(path: int):
-    """1: every later shifted call takes the slice-parallel streaming kernel;
-    0: the cluster kernel where it applies (the default)."""
+    """0 (the default): the cluster kernel where it is the faster path; 1:
+    every later shifted call takes the slice-parallel streaming kernel; 2:
+    the cluster kernel wherever it can run."""
     load().mhc_debug_set_decode_path(int(path))
 
 

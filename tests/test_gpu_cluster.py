@@ -5,8 +5,9 @@ summed in rank order), against the CPU oracle at the parity bar of the other
 paths: residual_out bit-exact, layer input within 1 bf16 ulp, coefficients
 within 1e-5 relative + 1e-7, mixes within 1e-5 of max(|mix|, ||terms||_2).
 Also: both decode paths (cluster and slice-parallel) on the same inputs,
-determinism, graph capture, the allocation-free entry point, and the shapes
-whose cluster sizes are not powers of two."""
+determinism, graph capture, the default path choice, and the shapes whose
+cluster sizes are not powers of two. These tests force the cluster kernel
+wherever it can run (by default it runs only where it is the faster path)."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +26,7 @@ def _lib():
     from manifold_constrained_hyper_gb300 import build
     build.build()
     ops.load()
-    ops.mhc_debug_set_decode_path(0)
+    ops.mhc_debug_set_decode_path(2)          # the cluster kernel wherever it can run
     yield
     ops.mhc_debug_set_decode_path(0)
 
@@ -124,7 +125,7 @@ def test_cluster_and_slice_paths_agree_and_are_deterministic(T):
     try:
         s = run_gpu("shifted", d, weight=w)
     finally:
-        ops.mhc_debug_set_decode_path(0)
+        ops.mhc_debug_set_decode_path(2)
     assert s["path"] == "slices" or ops.plan_cluster(T, 7168) == 0
     c = runs[0]
     assert torch.equal(c["residual_out_dev"], s["residual_out_dev"])
@@ -188,3 +189,19 @@ def test_cluster_calls_capture_and_replay_with_new_inputs(T):
         if a_.dtype == torch.bfloat16:
             a_, b_ = a_.view(torch.int16), b_.view(torch.int16)
         assert torch.equal(a_, b_)
+
+
+def test_default_path_choice():
+    """By default the cluster kernel takes the shapes where it is the faster
+    path: one chunk per CTA, or two for up to 16 tokens."""
+    ops.mhc_debug_set_decode_path(0)
+    try:
+        assert ops.plan_cluster(1, 256) == 8 and ops.plan_cluster(64, 512) == 16
+        assert ops.plan_cluster(8, 1024) == 16 and ops.plan_cluster(17, 1024) == 0
+        assert ops.plan_cluster(1, 7168) == 0 and ops.plan_cluster(64, 4096) == 0
+        d = synth.make_inputs(5, 512, seed=1900)
+        g = run_gpu("shifted", d)
+        assert g["path"] == "cluster"
+        compare("shifted", g, run_oracle("shifted", d))
+    finally:
+        ops.mhc_debug_set_decode_path(2)
