@@ -269,6 +269,21 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             if (kShifted) lv0 = __ldg(reinterpret_cast<const float4 *>(a.pre_lag) + gt0);
         }
     }
+    // the finishers' scale / base constants and (one thread) this call's
+    // flag value, loaded now so that their latency passes during the set-up
+    // (the decode variants' finisher warps issue the MMAs before they stage
+    // them)
+    float fin_const = 0.f;
+    unsigned long long fin_epoch = 0;
+    if (warp >= 12) {
+        const int i = tid - 12 * 32;
+        if (i < 3) fin_const = __ldg(a.coef.scale + i);
+        else if (i < 27) fin_const = __ldg(a.coef.base + i - 3);
+        if (tid == 12 * 32)
+            fin_epoch = a.epoch_cell != nullptr
+                            ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell) + 1
+                            : a.epoch;
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -797,14 +812,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // by that thread) shows that the CTA is done with the cell.
         volatile unsigned long long *epoch_sh =
             reinterpret_cast<volatile unsigned long long *>(gbase + kMiscOff + 48);
-        if (tid == 12 * 32)
-            *epoch_sh = a.epoch_cell != nullptr
-                            ? *reinterpret_cast<volatile const unsigned long long *>(a.epoch_cell) + 1
-                            : a.epoch;
+        if (tid == 12 * 32) *epoch_sh = fin_epoch;
         float *red = reinterpret_cast<float *>(gbase + kRedOff);
         float *rsum = red + kRsumOff;
         float *consts = red + kConstOff;
-        stage_coef_consts(a.coef, consts, tid - 12 * 32);
+        if (tid - 12 * 32 < 27) consts[tid - 12 * 32] = fin_const;   // scale[0..2], base[0..23]
         named_barrier_sync(kFinBarrier, kFinThreads);
         const unsigned long long epoch = *epoch_sh;
         const int t = q * 32 + lane;
@@ -1045,23 +1057,29 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             if (!kShifted) continue;
             float rstd_li = 0.f;
             if (a.fuse_coef) {
-                // single wave: the four finisher warps share the reduction. The
-                // tile's valid tokens form ntg groups of 32; each group's
-                // slices are cut into G = 4 / ntg consecutive ranges; warp w
-                // sums token group w % ntg over range w / ntg in slice order,
-                // and each token adds its G range sums in range order.
-                const long long tv = a.T - static_cast<long long>(it.tile) * kTileT;
-                const int ntg = tv >= kTileT ? 4 : static_cast<int>((tv + 31) / 32);
-                const int G = 4 / ntg;
-                const int tg = q % ntg, sg = q / ntg;
-                const long long gtok = static_cast<long long>(it.tile) * kTileT + tg * 32 + lane;
+                // single wave: the 128 finisher threads share the reduction.
+                // The tile's valid tokens, rounded up to a power of two (tvp),
+                // each get G = 128 / tvp threads; thread i takes token i % tvp
+                // and the i / tvp-th of G consecutive slice ranges, summed in
+                // slice order; each token adds its G range sums in range
+                // order. (With one thread per token a decode batch of a few
+                // tokens left almost every lane idle, and a token's loads went
+                // out one after another: 2.3 us at one token.)
+                const long long tvl = a.T - static_cast<long long>(it.tile) * kTileT;
+                const int tv = tvl >= kTileT ? kTileT : static_cast<int>(tvl);
+                int tvp = 1;
+                while (tvp < tv) tvp <<= 1;
+                const int G = kFinThreads / tvp;
+                const int ft = q * 32 + lane;
+                const int tk = ft % tvp, sg = ft / tvp;
                 float part = 0.f;
-                if (ok && a.norm_w != nullptr && sg < G && gtok < a.T) {
+                if (ok && a.norm_w != nullptr && tk < tv) {
                     const int per = (n_slices + G - 1) / G;
-                    const int s_end = (sg + 1) * per < n_slices ? (sg + 1) * per : n_slices;
-                    const float *pp = a.ssql + gtok;
+                    const int s_beg = sg * per;
+                    const int s_end = s_beg + per < n_slices ? s_beg + per : n_slices;
+                    const float *pp = a.ssql + static_cast<long long>(it.tile) * kTileT + tk;
                     const size_t step = static_cast<size_t>(a.T);
-                    for (int s2 = sg * per; s2 < s_end; s2 += 32) {
+                    for (int s2 = s_beg; s2 < s_end; s2 += 32) {
                         float vv[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) vv[i] = s2 + i < s_end ? __ldcg(pp + (s2 + i) * step) : 0.f;
@@ -1070,11 +1088,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             if (s2 + i < s_end) part += vv[i];
                     }
                 }
-                rsum[q * 32 + lane] = part;
+                rsum[ft] = part;
                 named_barrier_sync(kFinBarrier, kFinThreads);
                 if (ok && gt < a.T && a.norm_w != nullptr) {
                     float sl = 0.f;
-                    for (int g = 0; g < G; ++g) sl += rsum[(g * ntg + q) * 32 + lane];
+                    for (int g = 0; g < G; ++g) sl += rsum[g * tvp + t];
                     rstd_li = rsqrtf(__fdiv_rn(sl, static_cast<float>(a.H)) + a.coef.norm_eps);
                 }
             } else if (ok && gt < a.T && a.norm_w != nullptr) {
