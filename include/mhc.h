@@ -334,6 +334,22 @@ mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width)
  * three zero). Queries the device once per shape. */
 mhc_status mhc_plan_cluster(int64_t tokens, int hidden, int *ctas);
 
+/* Benchmark hook: enable = 0 launches the boundary kernels as plain stream
+ * kernels; nonzero (the default) as programmatic dependents of the previous
+ * kernel on the stream, whose set-up (barriers, tensor memory, descriptor and
+ * weight-tile prefetches into L2) overlaps that kernel's end while every
+ * read of global memory waits for its completion ("mhc_boundary" page,
+ * griddepcontrol around the kernel's prologue). Process-wide. */
+void mhc_debug_set_pdl(int enable);
+
+/* Test hook for the dependent launch: a kernel that lets the next kernel on
+ * `stream` start at once, waits delay_ns (at most 1,000,000, else
+ * MHC_ERR_SHAPE) and then copies n bf16 values from src to dst (device
+ * pointers, 16-byte aligned, not overlapping). The pages have no
+ * counterpart. */
+mhc_status mhc_debug_delayed_copy(const uint16_t *src, uint16_t *dst, int64_t n,
+                                  uint32_t delay_ns, void *stream);
+
 /* Test and benchmark hook for the shifted form's decode path, process-wide:
  * 0 (the default) as described at mhc_plan_cluster; 1 every later call takes
  * the slice-parallel streaming kernel; 2 every call that can take a cluster

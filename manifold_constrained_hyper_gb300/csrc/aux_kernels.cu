@@ -427,6 +427,29 @@ cudaError_t launch_post(const uint16_t *x, const uint16_t *res, const float *pos
     return cudaGetLastError();
 }
 
+namespace {
+// A producer for the programmatic-dependent-launch test: the next kernel on
+// the stream may launch at once; this one then waits delay_ns on the global
+// timer (bounded by the host at 1 ms) and only then writes dst, so that a
+// dependent that read dst before waiting for this grid would see old data.
+__global__ void delayed_copy_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                    long long n, uint32_t delay_ns) {
+    griddep_launch_dependents();
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < delay_ns) nanosleep_ns(200);
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        dst[i] = src[i];
+}
+}  // namespace
+
+cudaError_t launch_delayed_copy(const uint16_t *src, uint16_t *dst, long long n, uint32_t delay_ns,
+                                cudaStream_t s) {
+    // few blocks, so that the dependent's CTAs find free SMs while it waits
+    delayed_copy_kernel<<<4, 256, 0, s>>>(src, dst, n, delay_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>((a.T + kCoefTokens - 1) / kCoefTokens));

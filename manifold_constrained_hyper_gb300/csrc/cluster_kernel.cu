@@ -211,11 +211,22 @@ cluster_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant
         // expected before any peer can push (the cluster barrier below)
         mbar_arrive_expect_tx(part_bar, static_cast<uint32_t>(n_own * C * kClusterRecFloats * 4));
         mbar_arrive_expect_tx(sql_bar, static_cast<uint32_t>(C * T * 4));
+        // Launched as a programmatic dependent, the kernel may start while
+        // the previous kernel on the stream still runs: until
+        // griddepcontrol.wait nothing here reads global memory that kernel
+        // might write, but the first chunks' weight tiles are prefetched
+        // into L2 (a prefetch reads nothing into the CTA).
+        for (int g = 0; g < nch && g < NS; ++g)
+            bulk_prefetch_l2(a.weight + static_cast<size_t>(hidden_of(g) / kChunk) * kWBytes, kWBytes);
+        griddep_wait();
         // the first two chunks' loads now; the producer sends the others
         // once the set-up is done (one thread issuing every copy held the
         // whole CTA's set-up back by ~2.5 us at 14 chunks)
         for (int g = 0; g < nch && g < kEarlyLoads; ++g) issue_load(g);
     }
+    if (tid == 0) griddep_launch_dependents();
+    // every global read below may depend on the previous kernel
+    griddep_wait();
     if (tid < 27) stage_coef_consts(a.coef, consts, tid);
     __syncwarp();
     if (warp == 0) {
@@ -617,13 +628,21 @@ cudaError_t launch_cluster(const CUtensorMap &res, const CUtensorMap &x, const C
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = a.smem_bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = a.ctas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    int n = 1;
+    // a programmatic dependent of the previous kernel on the stream (the
+    // kernel waits for it before any read of global memory)
+    if (a.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, res, x, rout, a);
 }
 

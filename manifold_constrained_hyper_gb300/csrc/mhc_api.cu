@@ -272,6 +272,10 @@ bool encode_cached(int kind, CUtensorMap *m, const void *ptr, int H, long long T
     return ok;
 }
 
+// Whether the boundary kernels launch as programmatic dependents of the
+// previous kernel on the stream (a benchmark hook turns it off).
+std::atomic<int> g_pdl{1};
+
 // Decode path of the shifted form: 0 = a cluster where one fits and is the
 // faster, 1 = always the slice-parallel streaming kernel, 2 = a cluster
 // wherever one fits (test and benchmark hooks).
@@ -426,6 +430,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
             // the reduced mixes, after the epoch cell (the workspace holds
             // at least T x 128 bytes there for any plan)
             ca.mix_out = reinterpret_cast<float *>(ws8 + kCellBytes);
+            ca.pdl = g_pdl.load();
             if (mhc_status s = cuda_status(launch_cluster(m_res, m_x, m_rout, ca, st))) return s;
             if (t_between_event) {
                 cudaEvent_t ev = t_between_event;
@@ -470,6 +475,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.nw_bf16 = norm_dtype == MHC_BF16;
     sa.out32 = (reinterpret_cast<uintptr_t>(layer_input) & 31u) == 0;
     sa.box_rows = box_rows_for(T);
+    sa.pdl = g_pdl.load();
     sa.layer_input = layer_input;
     sa.pre_out = pre_out;
     sa.post_out = post_out;
@@ -689,6 +695,20 @@ mhc_status mhc_plan_cluster(int64_t tokens, int hidden, int *ctas) {
         (path == 2 || cluster_preferred(tokens, ca)) && cluster_fits(ca.ctas, ca.smem_bytes))
         *ctas = ca.ctas;
     return MHC_OK;
+}
+
+void mhc_debug_set_pdl(int enable) { g_pdl.store(enable ? 1 : 0); }
+
+mhc_status mhc_debug_delayed_copy(const uint16_t *src, uint16_t *dst, int64_t n,
+                                  uint32_t delay_ns, void *stream) {
+    if (n < 0 || delay_ns > 1000000u) return MHC_ERR_SHAPE;
+    if (n == 0) return MHC_OK;
+    if (!src || !dst) return MHC_ERR_NULL;
+    if (!aligned16(src) || !aligned16(dst)) return MHC_ERR_ALIGN;
+    if (overlap(src, static_cast<size_t>(n) * 2, dst, static_cast<size_t>(n) * 2)) return MHC_ERR_ALIAS;
+    DeviceInfo *dev = nullptr;
+    if (mhc_status s = current_device(&dev)) return s;
+    return cuda_status(launch_delayed_copy(src, dst, n, delay_ns, static_cast<cudaStream_t>(stream)));
 }
 
 void mhc_debug_set_decode_path(int path) { g_decode_path.store(path == 1 || path == 2 ? path : 0); }

@@ -76,6 +76,7 @@ struct StreamArgs {
                                  // streaming kernel); 0 otherwise
     int box_rows;                // one tile: token rows per residual / x box (the
                                  // residual maps then hold one stream per box); 0: 128
+    int pdl;                     // launch as a programmatic dependent of the previous kernel
 };
 
 struct FinishArgs {
@@ -133,6 +134,7 @@ struct ClusterArgs {
     float *pre_out, *post_out, *comb_out;
     float *mix_out;          // [T][kClusterRecFloats]: each token's reduced 24 mixes and
                              // 4H sum of squares, kept in the caller's scratch (or NULL)
+    int pdl;                 // launch as a programmatic dependent of the previous kernel
 };
 
 constexpr int kGridCap = 152;                       // persistent CTAs: one per GB300 SM
@@ -169,6 +171,10 @@ cudaError_t launch_unarmed_wait(unsigned int *status, unsigned long long timeout
 // shifted call that follows on the stream, when that call is being captured.
 cudaError_t launch_coef_check(const float *v, const CoefArgs &c, int H, long long n,
                               float *out_thread, float *out_lanes, cudaStream_t s);
+// Test producer: lets the next kernel on the stream start at once, waits
+// delay_ns (bounded), then copies n bf16 values src -> dst.
+cudaError_t launch_delayed_copy(const uint16_t *src, uint16_t *dst, long long n, uint32_t delay_ns,
+                                cudaStream_t s);
 cudaError_t launch_rcp_check(uint32_t first, unsigned long long count, unsigned long long *out,
                              cudaStream_t s);
 unsigned int *device_status_word();   // of the current device; NULL on failure

@@ -127,6 +127,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
         : "memory");
 }
+// Prefetch `bytes` (a multiple of 16, from a 16-byte aligned address) of
+// global memory into L2; nothing is written anywhere.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

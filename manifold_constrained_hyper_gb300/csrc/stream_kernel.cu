@@ -234,6 +234,18 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         mbar_init(end_full, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        // Launched as a programmatic dependent, the kernel may start while
+        // the previous kernel on the stream still runs: until
+        // griddepcontrol.wait nothing here reads global memory that kernel
+        // might write, but the first chunks' weight tiles are prefetched
+        // into L2 (a prefetch reads nothing into the CTA).
+        for (int g = 0; g < total && g < kStages; ++g) {
+            const Item it = item_of(g / d, n_slices);
+            bulk_prefetch_l2(a.weight + static_cast<size_t>(chunk_hidden(it.slice, g % d, n_slices) / kChunk) *
+                                            kWBytes,
+                             kWBytes);
+        }
+        griddep_wait();
         // the shifted form sends its first loads before the rest of the
         // set-up (the first stage landed ~3.5 us after the kernel started;
         // 0.4-0.9 us less from 768 to 8192 tokens at hidden 7168); the
@@ -249,9 +261,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         tmem_alloc(smem_addr(tmem_slot), kTmemCols);
         tmem_relinquish();
     }
-    // the finishing kernel launched after this one may start its blocks as
-    // soon as SMs free up; it waits for this grid's completion itself
+    // the kernel launched after this one may start its blocks as soon as
+    // SMs free up; it waits for this grid's completion itself
     if (tid == 0) griddep_launch_dependents();
+    // every global read below may depend on the previous kernel
+    griddep_wait();
     // the worker threads load the first item's coefficients of the previous
     // boundary now, while the set-up runs (at the start of the item their
     // latency delayed a decode call's first chunk by ~0.5 us)
@@ -1193,23 +1207,30 @@ cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtenso
         if (e != cudaSuccess) return e;
         opted.fetch_or(bit, std::memory_order_release);
     }
-    if (MODE != FUSED_SHIFTED && MODE != kShiftedDecode && MODE != kShiftedDecodeHalf &&
-        !a.fuse_coef) {
-        kern<<<grid, kThreads, smem, s>>>(res, x, rout, a, n_slices, n_items);
-        return cudaGetLastError();
-    }
-    // the shifted form's CTAs wait on one another (and the unshifted forms'
-    // when they form the coefficients): launch them co-resident
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    // the shifted form's CTAs wait on one another (and the unshifted forms'
+    // when they form the coefficients): launch them co-resident
+    if (MODE == FUSED_SHIFTED || MODE == kShiftedDecode || MODE == kShiftedDecodeHalf || a.fuse_coef) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    // a programmatic dependent of the previous kernel on the stream: its
+    // set-up overlaps that kernel's end (the kernel waits for it before any
+    // read of global memory)
+    if (a.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kern, res, x, rout, a, n_slices, n_items);
 }
 

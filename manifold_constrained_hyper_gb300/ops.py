@@ -28,7 +28,7 @@ EXPORTS = ("mhc_weight_bytes", "mhc_prepare_weight", "mhc_post", "mhc_workspace_
            "mhc_status_string", "mhc_set_wait_timeout_ns", "mhc_debug_unarmed_wait",
            "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc",
            "mhc_debug_rcp_check", "mhc_pre_split_k", "mhc_debug_coef_check", "mhc_plan_cluster",
-           "mhc_debug_set_decode_path")
+           "mhc_debug_set_decode_path", "mhc_debug_set_pdl", "mhc_debug_delayed_copy")
 
 
 class MhcError(RuntimeError):
@@ -97,6 +97,8 @@ def load():
         "mhc_plan": (i32, [i64, i32, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
         "mhc_plan_cluster": (i32, [i64, i32, ctypes.POINTER(ctypes.c_int)]),
         "mhc_debug_set_decode_path": (None, [i32]),
+        "mhc_debug_set_pdl": (None, [i32]),
+        "mhc_debug_delayed_copy": (i32, [P, P, i64, ctypes.c_uint32, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -183,6 +185,22 @@ def mhc_debug_set_decode_path(path: int):
     every later shifted call takes the slice-parallel streaming kernel; 2:
     the cluster kernel wherever it can run."""
     load().mhc_debug_set_decode_path(int(path))
+
+
+def mhc_debug_set_pdl(enable: bool):
+    """Launch the boundary kernels as programmatic dependents (the default)
+    or as plain stream kernels."""
+    load().mhc_debug_set_pdl(int(bool(enable)))
+
+
+def mhc_debug_delayed_copy(src, dst, delay_ns: int, stream=None):
+    """dst <- src (bf16, same size) by a kernel that lets the next kernel on
+    the stream start at once and writes only after delay_ns."""
+    _bf16(src, "src"), _bf16(dst, "dst")
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst must have the same size")
+    _check(load().mhc_debug_delayed_copy(_p(src), _p(dst), src.numel(), int(delay_ns),
+                                         _stream(stream, src.device)), "mhc_debug_delayed_copy")
 
 
 def mhc_prepare_weight(fn: torch.Tensor, out: torch.Tensor | None = None, stream=None):
