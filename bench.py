@@ -348,8 +348,14 @@ def measure_decode(dev, token_counts=None):
       back to back (the host's enqueue time is not counted);
     * eager_cold_l2: the same after a 256 MB buffer was written (L2 cold);
     * host_us_per_call: host time of one eager shifted call through the
-      Python binding and, apart, through the C entry point alone (ctypes
-      with its arguments prebuilt), mean over 200 calls."""
+      Python binding, through ctypes with its arguments prebuilt, and of the
+      C entry point alone (the ctypes time less that of a 0-token call, which
+      returns after its first checks), mean over 200 calls;
+    * pair_pdl / pair_no_pdl (1 and 64 tokens): a copy kernel producing x
+      followed by the call, per pair from a CUDA graph of 50 pairs, with the
+      boundary launched as a programmatic dependent of the producer or not.
+    The decode path of each size is the default one (cluster_ctas > 0: one
+    thread-block cluster; else the slice-parallel streaming kernel)."""
     import ctypes as ct
     import torch
     from manifold_constrained_hyper_gb300 import ops, synth
@@ -357,8 +363,8 @@ def measure_decode(dev, token_counts=None):
     H = synth.DECODE_HIDDEN
     scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = {"hidden": H, "unit": "us/call", "graph": {}, "graph_unshifted": {}, "graph_pre": {},
-           "eager_warm": {}, "eager_cold_l2": {}, "host_us_per_call": {}, "slices": {},
-           "waves": {}}
+           "eager_warm": {}, "eager_cold_l2": {}, "host_us_per_call": {}, "pair_pdl": {},
+           "pair_no_pdl": {}, "slices": {}, "cluster_ctas": {}, "waves": {}}
     sms = min(152, torch.cuda.get_device_properties(dev).multi_processor_count)
     for T in token_counts:
         cfg = synth.decode_workload(T)
@@ -396,18 +402,36 @@ def measure_decode(dev, token_counts=None):
                 ct.byref(p), T, H, outs["residual_out"].data_ptr(), outs["layer_input"].data_ptr(),
                 outs["pre_out"].data_ptr(), outs["post_out"].data_ptr(), outs["comb_out"].data_ptr(),
                 ws.data_ptr(), ws.numel(), cst]
+        # the same call with 0 tokens returns right after its first checks:
+        # its time is the ctypes marshalling of the 21 arguments alone
+        args0 = list(args)
+        args0[11] = 0
         host = {}
-        for kind in ("python", "c_entry"):
+        for kind in ("python", "c_entry_via_ctypes", "ctypes_only"):
             torch.cuda.synchronize()
             t0 = time.perf_counter()
             for _ in range(200):
                 if kind == "python":
                     call()
-                else:
+                elif kind == "c_entry_via_ctypes":
                     lib.mhc_boundary_fused(*args)
+                else:
+                    lib.mhc_boundary_fused(*args0)
             host[kind] = (time.perf_counter() - t0) / 200 * 1e6
             torch.cuda.synchronize()
+        host["c_entry"] = host["c_entry_via_ctypes"] - host["ctypes_only"]
         out["host_us_per_call"][str(T)] = host
+        # a producer of x (a copy kernel) and the boundary, replayed from a
+        # graph of 50 pairs, with the boundary a programmatic dependent of
+        # the producer (its set-up overlapping the producer's end) or not
+        if T in (1, 64):
+            x_src = ins["x"].clone()
+            pair_call = lambda st=None: (ops.mhc_debug_delayed_copy(x_src, ins["x"], 0, stream=st),
+                                         call(st))
+            for pdl in (1, 0):
+                ops.mhc_debug_set_pdl(pdl)
+                out["pair_pdl" if pdl else "pair_no_pdl"][str(T)] = _graph_us(pair_call, 50, dev)
+            ops.mhc_debug_set_pdl(1)
         key = str(T)
         out["graph"][key] = _graph_us(call, 100, dev)
         for form in ("unshifted", "pre"):
@@ -416,6 +440,7 @@ def measure_decode(dev, token_counts=None):
         out["eager_cold_l2"][key] = statistics.median(cold)
         S, _ = ops.plan(T, H)
         out["slices"][key] = S
+        out["cluster_ctas"][key] = ops.plan_cluster(T, H)
         out["waves"][key] = -(-((T + 127) // 128 * S) // sms)
     if ops.mhc_get_device_status() != 0:
         raise RuntimeError("device-side wait timed out during the decode sweep")
