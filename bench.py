@@ -549,6 +549,8 @@ def run_ours(args):
     cfg = dict(synth.WORKLOADS[args.workload])
     if args.tokens:
         cfg["T"] = args.tokens
+    if args.hidden:
+        cfg["H"] = args.hidden
     T, H = cfg["T"], cfg["H"]
     extra = {k: v for k, v in cfg.items() if k not in ("T", "H", "seed")}
     d = synth.make_inputs_device(T, H, rank_seed(cfg["seed"], rank), dev, **extra)
@@ -702,6 +704,7 @@ def run_ours(args):
         "data": "synthetic (seeded; residual/x ~ N(0,1) bf16, doubly stochastic comb)",
         "config": {"workload": args.workload, "tokens": T, "hidden": H, "n_hc": 4,
                    "variant": "shifted fused boundary", "sinkhorn_iters": 20,
+                   "decode_path": "cluster" if ops.plan_cluster(T, H) else "slice-parallel",
                    "norm_w": "fp32", "hidden_slices": S, "slice_width": sw,
                    "l2": "inputs larger than L2 (no flush); prepared mixer L2-resident",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
@@ -742,6 +745,9 @@ def main():
     ap.add_argument("--reference-tokens", type=int, default=256)
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (profiling a smaller case)")
+    ap.add_argument("--hidden", type=int, default=0,
+                    help="override the workload's hidden size (profiling another kernel: a "
+                         "shifted call of up to 16 tokens at hidden 512 takes the cluster kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
