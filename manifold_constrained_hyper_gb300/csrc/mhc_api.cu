@@ -476,6 +476,9 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     sa.out32 = (reinterpret_cast<uintptr_t>(layer_input) & 31u) == 0;
     sa.box_rows = box_rows_for(T);
     sa.pdl = g_pdl.load();
+    sa.collapse_in_kernel = 0;
+    sa.res_in = residual;
+    sa.x_in = x;
     sa.layer_input = layer_input;
     sa.pre_out = pre_out;
     sa.post_out = post_out;
@@ -502,6 +505,11 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     const bool one_round = tiles == 1 && (T + S - 1) / S <= kRoundTok;
     sa.fuse_coef = items <= grid && !invariant && (mode == FUSED_SHIFTED || one_round);
     sa.coef_end = mode == FUSED_SHIFTED && !sa.fuse_coef;
+    // the unshifted forms of a single wave write the layer input in the
+    // streaming kernel too (the owner CTA recomputes each of its tokens'
+    // updated residual from the inputs, so not when the update is in place)
+    sa.collapse_in_kernel = mode != FUSED_SHIFTED && sa.fuse_coef && H <= kInKernelCollapseMaxH &&
+                            !(mode == FUSED_UNSHIFTED && residual_out == residual);
     sa.decode_map = mode == FUSED_SHIFTED && sa.fuse_coef && T <= kDecodeMaxTokens &&
                             w / kChunk <= kStreamStages
                         ? (T <= 32 ? 1 : 2)
@@ -546,7 +554,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     fa.comb_out = comb_out;
     fa.T = T;
     fa.H = H;
-    if (mode == FUSED_SHIFTED) return MHC_OK;
+    if (mode == FUSED_SHIFTED || sa.collapse_in_kernel) return MHC_OK;
     if (!sa.fuse_coef)
         if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
     return cuda_status(launch_collapse_unshifted(fa, st));

@@ -77,7 +77,18 @@ struct StreamArgs {
     int box_rows;                // one tile: token rows per residual / x box (the
                                  // residual maps then hold one stream per box); 0: 128
     int pdl;                     // launch as a programmatic dependent of the previous kernel
+    // unshifted forms, single wave (fuse_coef), H <= kInKernelCollapseMaxH and not in place:
+    // each owner CTA also writes its tokens' layer input (no collapse kernel after it),
+    // recomputing the token's updated residual from the inputs
+    int collapse_in_kernel;
+    const uint16_t *res_in;      // [T,4,H] the residual input
+    const uint16_t *x_in;        // [T,H] the layer output (fused form)
 };
+
+// Largest hidden size whose unshifted single-wave calls collapse in the
+// streaming kernel (each of the owner CTA's 256 worker threads keeps up to
+// 4 units of 8 collapse values of the token in registers).
+constexpr int kInKernelCollapseMaxH = 8 * 256 * 4;
 
 struct FinishArgs {
     const float *partials;   // [tiles][n_slices] value-major item blocks of kItemFloats

@@ -96,6 +96,18 @@ enum : int { SITE_PROD_READY = 1, SITE_PROD_MMA = 2, SITE_MMA_FULL = 3, SITE_MMA
              SITE_FIN_SUMS = 9, SITE_WORK_SUMS = 10, SITE_TILE_FLAGS = 11, SITE_WORK_LI = 12,
              SITE_WORK_COEF = 14, SITE_EPOCH = 15 };
 
+// AND of `v` over the 256 worker threads (named barrier kWorkBarrier = 2);
+// every worker warp must call it.
+__device__ __forceinline__ bool workers_and(bool v) {
+    uint32_t r;
+    __syncwarp();
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 2, 256, p;\n"
+        "selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r) : "r"(static_cast<uint32_t>(v)) : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void regs_dec_producer() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
 }
@@ -783,6 +795,85 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                                          a.comb_out);
                 }
                 named_barrier_sync(kWorkBarrier, kWorkThreads);
+            }
+            // ---- unshifted forms, one kernel: the owner CTA writes the
+            // layer input of each token whose coefficients it formed. Its
+            // worker threads recompute the token's updated residual over the
+            // whole hidden dimension from the inputs (the same chain as the
+            // streaming pass, so bit for bit the stored residual; pre-only:
+            // the residual itself), collapse it with this boundary's pre
+            // (written above by this CTA), add the collapse's squares in a
+            // fixed order (per thread, then a warp tree, then the warps in
+            // order) and normalise. No second kernel, and no exchange
+            // between CTAs beyond the coefficients'.
+            if (!kShifted && a.collapse_in_kernel) {
+                float *wsum = red;                               // [8] warp sums
+                const int units = a.H / 8;
+                ok = workers_and(ok);                            // one verdict for every worker warp
+                for (int j = 0; j < ntok; ++j) {
+                    const long long tok = gbase_t + static_cast<long long>(n_slices) * j;
+                    if (!ok || tok >= a.T) break;                // the same for every worker
+                    const float4 pv = reinterpret_cast<const float4 *>(a.pre_out)[tok];
+                    Coefs c;
+                    const float ps4[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) c.pre2[i] = f2_pack(ps4[i], ps4[i]);
+                    if (MODE != PRE_ONLY) {
+                        const float4 qv = __ldg(reinterpret_cast<const float4 *>(a.post) + tok);
+                        float4 cq[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) cq[i] = __ldg(reinterpret_cast<const float4 *>(a.comb) + tok * 4 + i);
+                        const Coefs u = coefs_of(qv, cq, pv);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) c.post2[i] = u.post2[i];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int k2 = 0; k2 < 4; ++k2) c.comb2[i][k2] = u.comb2[i][k2];
+                    }
+                    uint4 lis[4];
+                    uint64_t sq = 0;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int u = wt + kWorkThreads * k;
+                        lis[k] = make_uint4(0u, 0u, 0u, 0u);
+                        if (u < units) {
+                            const long long h0 = 8LL * u;
+                            uint4 r[4], cur[4];
+#pragma unroll
+                            for (int s2 = 0; s2 < 4; ++s2) r[s2] = ld_global_nc_v4(a.res_in + (tok * 4 + s2) * a.H + h0);
+                            if (MODE != PRE_ONLY) {
+                                update8(r, ld_global_nc_v4(a.x_in + tok * a.H + h0), c, cur);
+                            } else {
+#pragma unroll
+                                for (int s2 = 0; s2 < 4; ++s2) cur[s2] = r[s2];
+                            }
+                            lis[k] = collapse8(cur, c);
+                            sq_accum(lis[k], sq);
+                        }
+                    }
+                    float sw = f2_lo(sq) + f2_hi(sq);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
+                    if (lane == 0) wsum[warp - 4] = sw;
+                    named_barrier_sync(kWorkBarrier, kWorkThreads);
+                    float tot = 0.f;
+#pragma unroll
+                    for (int w2 = 0; w2 < kWorkThreads / 32; ++w2) tot += wsum[w2];
+                    const float rstd_li = rsqrtf(__fdiv_rn(tot, static_cast<float>(a.H)) + a.coef.norm_eps);
+                    uint16_t *row = a.layer_input + tok * a.H;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int u = wt + kWorkThreads * k;
+                        if (u < units) {
+                            const uint4 o = a.norm_w == nullptr
+                                                ? lis[k]
+                                                : norm8(lis[k], rstd_li, a.norm_w, a.nw_bf16, 8LL * u);
+                            *reinterpret_cast<uint4 *>(row + 8LL * u) = o;
+                        }
+                    }
+                    named_barrier_sync(kWorkBarrier, kWorkThreads);   // wsum reused
+                }
             }
         }
         tc_fence_before();

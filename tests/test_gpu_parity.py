@@ -500,3 +500,17 @@ def test_unarmed_wait_times_out_and_context_survives():
         ops.mhc_set_wait_timeout_ns(0)
     d = synth.make_inputs(4, 256, seed=404)
     compare("shifted", run_gpu("shifted", d), run_oracle("shifted", d))
+
+
+@pytest.mark.parametrize("mode,T,H,in_place", [("unshifted", 5, 7168, True), ("unshifted", 3, 16384, False),
+                                               ("pre", 3, 16384, False), ("unshifted", 40, 8192, False),
+                                               ("pre", 128, 8192, False)])
+def test_unshifted_single_wave_collapse_paths(mode, T, H, in_place):
+    """Unshifted single-wave calls write the layer input in the streaming
+    kernel up to hidden 8192 (the owner CTA recomputes each token's updated
+    residual); in place, or above hidden 8192, the collapse kernel still
+    follows. Both against the oracle."""
+    d = synth.make_inputs(T, H, seed=2100 + T + H)
+    g = run_gpu(mode, d, in_place=in_place)
+    o = run_oracle(mode, d)
+    compare(mode, g, o, d=d)
