@@ -495,14 +495,17 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // its workers: in a single wave of items as soon as the tile has
     // published (reduction split into ranges, for latency), otherwise after
     // the CTA's last item (reduction in slice order, as in the
-    // batch-invariant plan). The unshifted forms do so for a single wave of
-    // one tile whose CTAs have one round of tokens each (kRoundTok), and
-    // then a kernel writes the layer input: at 1 to 128 tokens and hidden
-    // 7168 that took 0.4-2.4 us less than the coefficients kernel between
-    // the two. With several rounds per CTA the in-kernel reduction, which
-    // the layer-input kernel waits for, grows with them; those calls keep
-    // the coefficients kernel.
-    const bool one_round = tiles == 1 && (T + S - 1) / S <= kRoundTok;
+    // batch-invariant plan). The unshifted forms do so for a single wave
+    // whose CTAs own one round of tokens each (kRoundTok) of their tile,
+    // and their owner CTAs then write those tokens' layer input too
+    // (collapse_in_kernel; else a collapse kernel follows): at 1 to 128
+    // tokens and hidden 7168 forming them in-kernel took 0.4-2.4 us less
+    // than the coefficients kernel between the two. With several rounds per
+    // CTA the in-kernel reduction grows with them; those calls keep the
+    // coefficients kernel.
+    // (every tile but a single one has 128 tokens)
+    const long long tile_tokens = tiles == 1 ? T : kTileT;
+    const bool one_round = (tile_tokens + S - 1) / S <= kRoundTok;
     sa.fuse_coef = items <= grid && !invariant && (mode == FUSED_SHIFTED || one_round);
     sa.coef_end = mode == FUSED_SHIFTED && !sa.fuse_coef;
     // the unshifted forms of a single wave write the layer input in the
