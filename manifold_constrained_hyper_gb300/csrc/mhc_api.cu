@@ -495,17 +495,20 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // its workers: in a single wave of items as soon as the tile has
     // published (reduction split into ranges, for latency), otherwise after
     // the CTA's last item (reduction in slice order, as in the
-    // batch-invariant plan). The unshifted forms do so for a single wave
-    // whose CTAs own one round of tokens each (kRoundTok) of their tile,
-    // and their owner CTAs then write those tokens' layer input too
+    // batch-invariant plan). The unshifted forms do so for a single wave of
+    // one tile whose CTAs own one round of tokens each (kRoundTok), and the
+    // owner CTAs then write those tokens' layer input too
     // (collapse_in_kernel; else a collapse kernel follows): at 1 to 128
     // tokens and hidden 7168 forming them in-kernel took 0.4-2.4 us less
     // than the coefficients kernel between the two. With several rounds per
     // CTA the in-kernel reduction grows with them; those calls keep the
     // coefficients kernel.
-    // (every tile but a single one has 128 tokens)
-    const long long tile_tokens = tiles == 1 ? T : kTileT;
-    const bool one_round = (tile_tokens + S - 1) / S <= kRoundTok;
+    // (several tiles in one wave measured slower in-kernel: at 512 and 256
+    // tokens, hidden 7168, 24.3 / 20.3 us unshifted with the coefficients in
+    // the streaming kernel and a collapse kernel, 30.4 / 24.4 us with the
+    // owners also writing the layer input, against 22.1 / 18.8 us with the
+    // coefficients kernel between the two)
+    const bool one_round = tiles == 1 && (T + S - 1) / S <= kRoundTok;
     sa.fuse_coef = items <= grid && !invariant && (mode == FUSED_SHIFTED || one_round);
     sa.coef_end = mode == FUSED_SHIFTED && !sa.fuse_coef;
     // the unshifted forms of a single wave write the layer input in the

@@ -87,7 +87,7 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
     # mixes, then the 4H sum of squares), in a block of 128 x 32 floats per
     # (128-token tile, slice) item: token-major [128][28] when the streaming
     # kernel's workers reduce them (a single wave of items; for the unshifted
-    # forms only when each CTA owns at most 5 tokens of its tile, one round);
+    # forms only one tile whose CTAs have at most 5 tokens each, one round);
     # value-major [25][128] in the other unshifted calls; otherwise (shifted,
     # several items per CTA) one 32-float record per token and slice,
     # [tiles * 128][S][32]
@@ -96,8 +96,7 @@ def run_gpu(mode: str, d: dict, norm: str = "f32", params: ops.Params | None = N
     # (the partials start 256 bytes into the workspace, after the epoch cell)
     raw = ws[256: 256 + tiles * S * 32 * 128 * 4].view(torch.float32).view(tiles, S, 32 * 128)
     single_wave = tiles * S <= sms and not (params and params.batch_invariant)
-    tile_tokens = T if tiles == 1 else 128
-    in_kernel = single_wave and (mode == "shifted" or -(-tile_tokens // S) <= 5)
+    in_kernel = single_wave and (mode == "shifted" or (tiles == 1 and -(-T // S) <= 5))
     if in_kernel:
         blk = raw[..., : 128 * 28].reshape(tiles, S, 128, 28)[..., :25].permute(1, 0, 2, 3)
     elif mode == "shifted":
