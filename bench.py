@@ -71,8 +71,8 @@ def alg_bytes_form(form: str, T: int, H: int) -> int:
 # of the full-size workload, each with the hash of the kernel sources it was
 # taken on (source_hash()). A figure whose hash no longer matches the
 # sources being run is not reported: the kernel has changed since.
-STREAM_KERNEL_TRAFFIC = {(8192, 7168): (597.98e6 + 540.99e6, "8eb0c97c34a5be54")}
-KERNEL_SOURCES = ("stream_kernel.cu", "ptx.cuh", "coef.cuh", "mhc_internal.h")
+STREAM_KERNEL_TRAFFIC = {(8192, 7168): (598.04e6 + 540.75e6, "a55a8db266d5f0e4")}
+KERNEL_SOURCES = ("stream_kernel.cu", "ptx.cuh", "coef.cuh", "elementwise.cuh", "mhc_internal.h")
 
 
 def source_hash() -> str:
@@ -345,8 +345,11 @@ def measure_decode(dev, token_counts=None):
       amortised, L2 warm as in a decode loop);
     * eager_warm: device time of one eager shifted call with L2 warm, its
       events and the call enqueued behind a short GPU sleep so that they run
-      back to back (the host's enqueue time is not counted);
-    * eager_cold_l2: the same after a 256 MB buffer was written (L2 cold);
+      back to back (the host's enqueue time is not counted); the mean over
+      60 calls (one call's event pair reads on a coarse grid, in steps of
+      about 2 us, so a median would be a grid value);
+    * eager_cold_l2: the same after a 256 MB buffer was written (L2 cold),
+      mean over 30 calls;
     * host_us_per_call: host time of one eager shifted call through the
       Python binding, through ctypes with its arguments prebuilt, and of the
       C entry point alone (the ctypes time less that of a 0-token call, which
@@ -377,21 +380,21 @@ def measure_decode(dev, token_counts=None):
             call()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(50)]
+              for _ in range(90)]
         for a, b in ev:
             a.record()
             b.record()
         torch.cuda.synchronize()
         warm, cold = [], []
         for i, (a, b) in enumerate(ev):
-            if i < 20:
+            if i < 30:
                 scrub.add_(1)
             torch.cuda._sleep(100_000)               # the GPU waits while the host enqueues
             a.record()
             call()
             b.record()
             torch.cuda.synchronize()
-            (cold if i < 20 else warm).append(a.elapsed_time(b) * 1e3)
+            (cold if i < 30 else warm).append(a.elapsed_time(b) * 1e3)
         # host time per call: Python binding, then the C entry point alone
         lib = ops.load()
         p = ops.Params().c()
@@ -436,8 +439,8 @@ def measure_decode(dev, token_counts=None):
         out["graph"][key] = _graph_us(call, 100, dev)
         for form in ("unshifted", "pre"):
             out["graph_" + form][key] = _graph_us(_boundary_call(form, ins, outs, ws), 100, dev)
-        out["eager_warm"][key] = statistics.median(warm)
-        out["eager_cold_l2"][key] = statistics.median(cold)
+        out["eager_warm"][key] = statistics.fmean(warm)
+        out["eager_cold_l2"][key] = statistics.fmean(cold)
         S, _ = ops.plan(T, H)
         out["slices"][key] = S
         out["cluster_ctas"][key] = ops.plan_cluster(T, H)

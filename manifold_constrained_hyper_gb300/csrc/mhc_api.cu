@@ -516,7 +516,11 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // updated residual from the inputs, so not when the update is in place)
     sa.collapse_in_kernel = mode != FUSED_SHIFTED && sa.fuse_coef && H <= kInKernelCollapseMaxH &&
                             !(mode == FUSED_UNSHIFTED && residual_out == residual);
-    sa.decode_map = mode == FUSED_SHIFTED && sa.fuse_coef && T <= kDecodeMaxTokens &&
+    // the decode worker mapping (every worker warp on a quarter or half of
+    // each hidden unit) for a single wave of one tile of at most 64 tokens
+    // whose items fit the stages, in the fused forms (unshifted: 0.6-1.2 us
+    // less at hidden 7168, 1 to 64 tokens)
+    sa.decode_map = mode != PRE_ONLY && sa.fuse_coef && tiles == 1 && T <= kDecodeMaxTokens &&
                             w / kChunk <= kStreamStages
                         ? (T <= 32 ? 1 : 2)
                         : 0;

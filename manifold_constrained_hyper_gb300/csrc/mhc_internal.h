@@ -69,10 +69,10 @@ struct StreamArgs {
     int fuse_coef;               // one item per CTA: the workers form the coefficients
     int coef_end;                // shifted, several items per CTA: the workers form
                                  // them after the CTA's last item (record layout)
-    int decode_map;              // shifted, one tile of at most kDecodeMaxTokens tokens in
-                                 // a single wave, at most kStreamStages chunks: the decode
-                                 // mapping of the worker warps, 1 up to 32 tokens, 2 above,
-                                 // the collapse kept in the stage's x tile (see the
+    int decode_map;              // one tile of at most kDecodeMaxTokens tokens in a single
+                                 // wave, at most kStreamStages chunks, fused forms: the decode
+                                 // mapping of the worker warps, 1 up to 32 tokens, 2 above
+                                 // (shifted: the collapse kept in the stage's x tile; see the
                                  // streaming kernel); 0 otherwise
     int box_rows;                // one tile: token rows per residual / x box (the
                                  // residual maps then hold one stream per box); 0: 128

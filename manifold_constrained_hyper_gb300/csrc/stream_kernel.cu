@@ -49,11 +49,15 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kStages = kStreamStages;
-// Template values of the shifted form's decode variants (the decode worker
-// mapping, chosen by the host through StreamArgs::decode_map): up to 32
-// tokens (quarter units) and 33 to kDecodeMaxTokens tokens (whole units).
+// Template values of the decode variants (the decode worker mapping, chosen
+// by the host through StreamArgs::decode_map) of the two fused forms: up to
+// 32 tokens (quarter units) and 33 to kDecodeMaxTokens tokens (whole units).
+// (The pre-only form has no update to spread: with the mapping its decode
+// calls measured 0.1-0.35 us slower at hidden 7168, 1 to 64 tokens.)
 constexpr int kShiftedDecode = 3;
 constexpr int kShiftedDecodeHalf = 4;
+constexpr int kUnshiftedDecode = 5;
+constexpr int kUnshiftedDecodeHalf = 6;
 constexpr int kBarOff = kStages * kStageBytes;
 constexpr int kAccBufs = 2;                            // accumulator / sums buffers
 constexpr int kLiBufs = 3;                             // shifted: collapse buffers
@@ -149,8 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant__ CUtensorMap tm_x,
               const __grid_constant__ CUtensorMap tm_rout, const StreamArgs a, int n_slices,
               int n_items) {
-    constexpr bool kDecodeMap = MODE == kShiftedDecode || MODE == kShiftedDecodeHalf;
-    constexpr bool kShifted = MODE == FUSED_SHIFTED || kDecodeMap;
+    constexpr bool kDecodeMap = MODE >= kShiftedDecode;
+    // the form (PRE_ONLY, FUSED_UNSHIFTED or FUSED_SHIFTED) and, for the decode
+    // variants, whether tokens 33 to 64 are mapped (whole units per lane)
+    constexpr int kBase = !kDecodeMap ? MODE : (MODE <= kShiftedDecodeHalf ? FUSED_SHIFTED : FUSED_UNSHIFTED);
+    constexpr bool kHalfMap = MODE == kShiftedDecodeHalf || MODE == kUnshiftedDecodeHalf;
+    constexpr bool kShifted = kBase == FUSED_SHIFTED;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -190,7 +198,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     // 8192 x 7168, with the same DRAM bytes), the weight tile kept in L2.
     const uint64_t pol_load = policy_evict_normal();
     const uint64_t pol_keep = policy_evict_last();
-    constexpr uint32_t kLoadBytes = kResBytes + kWBytes + (MODE != PRE_ONLY ? kXBytes : 0);
+    constexpr uint32_t kLoadBytes = kResBytes + kWBytes + (kBase != PRE_ONLY ? kXBytes : 0);
     // A call of one tile (box_rows != 0) loads only the first box_rows token
     // rows of each stream, one box per stream into the same place of the
     // stage: the copy engine spends time on every row of a box, filled or
@@ -199,7 +207,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     const int box_rows = a.box_rows;
     const uint32_t load_bytes =
         box_rows == 0 ? kLoadBytes
-                      : kWBytes + (MODE != PRE_ONLY ? 5u : 4u) * static_cast<uint32_t>(box_rows) * kRowBytes;
+                      : kWBytes + (kBase != PRE_ONLY ? 5u : 4u) * static_cast<uint32_t>(box_rows) * kRowBytes;
     auto issue_load = [&](int g) {
         const int st = g % kStages;
         const uint32_t sb = base + st * kStageBytes;
@@ -214,7 +222,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             for (int s = 0; s < 4; ++s)
                 tma_load_3d(sb + s * kTileT * kRowBytes, &tm_res, hc, t0, s, full(st), pol_load);
         }
-        if (MODE != PRE_ONLY) tma_load_2d(sb + kResBytes, &tm_x, hc, t0, full(st), pol_load);
+        if (kBase != PRE_ONLY) tma_load_2d(sb + kResBytes, &tm_x, hc, t0, full(st), pol_load);
         bulk_load(sb + kResBytes + kXBytes, a.weight + static_cast<size_t>(hc / kChunk) * kWBytes,
                   kWBytes, full(st), pol_keep);
     };
@@ -225,7 +233,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     // the two took 1.2 us of a decode call).
     if (tid == 32) {
         tma_prefetch_desc(&tm_res);
-        if (MODE != PRE_ONLY) { tma_prefetch_desc(&tm_x); tma_prefetch_desc(&tm_rout); }
+        if (kBase != PRE_ONLY) { tma_prefetch_desc(&tm_x); tma_prefetch_desc(&tm_rout); }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(full(i), 1);
             mbar_init(ready(i), 8);
@@ -286,9 +294,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     // (the decode mapping: token lane of the one tile)
     float4 pv0 = make_float4(0.f, 0.f, 0.f, 0.f), lv0 = pv0;
     float4 cv0[4] = {pv0, pv0, pv0, pv0};
-    if (MODE != PRE_ONLY && warp >= 4 && warp < 12 && n_local > 0) {
+    if (kBase != PRE_ONLY && warp >= 4 && warp < 12 && n_local > 0) {
         const long long gt0 = static_cast<long long>(item_of(0, n_slices).tile) * kTileT +
-                              (kDecodeMap ? (MODE == kShiftedDecodeHalf ? ((warp - 4) & 1) * 32 : 0)
+                              (kDecodeMap ? (kHalfMap ? ((warp - 4) & 1) * 32 : 0)
                                           : (warp & 3) * 32) + lane;
         if (gt0 < a.T) {
             pv0 = __ldg(reinterpret_cast<const float4 *>(a.post) + gt0);
@@ -334,7 +342,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 const int st = g % kStages;
                 const uint32_t ph = (g / kStages) & 1;
                 if (!mbar_wait(ready(st), ph, abort_flag, tmo, a.status, SITE_PROD_READY)) break;
-                if (MODE != PRE_ONLY) {
+                if (kBase != PRE_ONLY) {
                     const uint32_t sb = base + st * kStageBytes;
                     const Item it = item_of(g / d, n_slices);
                     const int hc = chunk_hidden(it.slice, g % d, n_slices);
@@ -352,7 +360,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 // whole chunk to read shared memory
                 if (g >= 1 && loaded < total) {
                     const int gp = g - 1;
-                    if (MODE != PRE_ONLY) bulk_wait_read_allbut1();
+                    if (kBase != PRE_ONLY) bulk_wait_read_allbut1();
                     if (!mbar_wait(mma_done(gp % kStages), (gp / kStages) & 1, abort_flag, tmo,
                                    a.status, SITE_PROD_MMA))
                         break;
@@ -487,16 +495,16 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // have tokens. Here worker warp w' = warp - 4 takes hidden unit w' / 2
         // of every chunk: of token lane, pairs 2 (w' % 2) and 2 (w' % 2) + 1
         // (up to 32 tokens: a quarter of the usual work per thread), or whole
-        // for token lane + 32 (w' % 2) (33 to 64 tokens: half). The collapse goes
-        // into the chunk's x tile (consumed by
-        // then, and read by neither the copy out nor the MMA) instead of TMEM,
-        // whose lane quarters belong to fixed warps; the finishers read it
-        // there. The per-token sums of squares are handed over per warp.
+        // for token lane + 32 (w' % 2) (33 to 64 tokens: half). The shifted
+        // form's collapse goes into the chunk's x tile (consumed by then, and
+        // read by neither the copy out nor the MMA) instead of TMEM, whose
+        // lane quarters belong to fixed warps; the finishers read it there.
+        // The per-token sums of squares are handed over per warp.
         constexpr bool dmap = kDecodeMap;
         if (dmap && total > 0) {
             // up to 32 tokens: warp w' takes unit w' / 2, pair-half w' % 2, of
             // token lane; 33 to 64: unit w' / 2 whole, of token lane + 32 (w' % 2)
-            constexpr bool quarter = MODE == kShiftedDecode;
+            constexpr bool quarter = !kHalfMap;
             const int wq = warp - 4, un = wq >> 1, pq = wq & 1;
             const int tt = quarter ? lane : lane + 32 * pq;
             const Coefs cd = coefs_of(pv0, cv0, lv0);      // token tt's, loaded in the set-up
@@ -517,9 +525,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             st_shared_v2(sb + s2 * kTileT * kRowBytes + off, cur[s2]);
                             sq_accum2(cur[s2], sq);
                         }
-                        const uint2 li = collapse4(cur, cd);
-                        st_shared_v2(sb + kResBytes + off, li);
-                        sq_accum2(li, sql);
+                        if (kShifted) {
+                            const uint2 li = collapse4(cur, cd);
+                            st_shared_v2(sb + kResBytes + off, li);
+                            sq_accum2(li, sql);
+                        }
                     } else {
                         uint4 r[4], cur[4];
 #pragma unroll
@@ -530,9 +540,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             st_shared_v4(sb + s2 * kTileT * kRowBytes + unit, cur[s2]);
                             sq_accum(cur[s2], sq);
                         }
-                        const uint4 li = collapse8(cur, cd);
-                        st_shared_v4(sb + kResBytes + unit, li);
-                        sq_accum(li, sql);
+                        if (kShifted) {
+                            const uint4 li = collapse8(cur, cd);
+                            st_shared_v4(sb + kResBytes + unit, li);
+                            sq_accum(li, sql);
+                        }
                     }
                 }
                 fence_proxy_async_smem();
@@ -560,7 +572,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 const Item it = item_of(k, n_slices);
                 const long long gt = static_cast<long long>(it.tile) * kTileT + t;
                 valid = gt < a.T;
-                if (MODE != PRE_ONLY) {
+                if (kBase != PRE_ONLY) {
                     // item 0's were loaded during the set-up
                     const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
                     float4 pv = k == 0 ? pv0 : z;
@@ -609,7 +621,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
                         r[s] = ld_shared_v4(sb + s * kTileT * kRowBytes + off);
-                    if (MODE == PRE_ONLY) {
+                    if (kBase == PRE_ONLY) {
 #pragma unroll
                         for (int s = 0; s < 4; ++s) sq_accum(r[s], ssq2);
                     } else {
@@ -818,7 +830,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     const float ps4[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) c.pre2[i] = f2_pack(ps4[i], ps4[i]);
-                    if (MODE != PRE_ONLY) {
+                    if (kBase != PRE_ONLY) {
                         const float4 qv = __ldg(reinterpret_cast<const float4 *>(a.post) + tok);
                         float4 cq[4];
 #pragma unroll
@@ -842,7 +854,7 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             uint4 r[4], cur[4];
 #pragma unroll
                             for (int s2 = 0; s2 < 4; ++s2) r[s2] = ld_global_nc_v4(a.res_in + (tok * 4 + s2) * a.H + h0);
-                            if (MODE != PRE_ONLY) {
+                            if (kBase != PRE_ONLY) {
                                 update8(r, ld_global_nc_v4(a.x_in + tok * a.H + h0), c, cur);
                             } else {
 #pragma unroll
@@ -1309,7 +1321,7 @@ cudaError_t launch_t(const CUtensorMap &res, const CUtensorMap &x, const CUtenso
     int n = 0;
     // the shifted form's CTAs wait on one another (and the unshifted forms'
     // when they form the coefficients): launch them co-resident
-    if (MODE == FUSED_SHIFTED || MODE == kShiftedDecode || MODE == kShiftedDecodeHalf || a.fuse_coef) {
+    if (MODE == FUSED_SHIFTED || (MODE >= kShiftedDecode && MODE <= kShiftedDecodeHalf) || a.fuse_coef) {
         attr[n].id = cudaLaunchAttributeCooperative;
         attr[n].val.cooperative = 1;
         ++n;
@@ -1337,6 +1349,10 @@ cudaError_t launch_stream(int mode, const CUtensorMap &res, const CUtensorMap &x
     switch (mode) {
         case PRE_ONLY: return launch_t<PRE_ONLY>(res, x, rout, a, n_slices, n_items, grid, s);
         case FUSED_UNSHIFTED:
+            if (a.decode_map == 1)
+                return launch_t<kUnshiftedDecode>(res, x, rout, a, n_slices, n_items, grid, s);
+            if (a.decode_map == 2)
+                return launch_t<kUnshiftedDecodeHalf>(res, x, rout, a, n_slices, n_items, grid, s);
             return launch_t<FUSED_UNSHIFTED>(res, x, rout, a, n_slices, n_items, grid, s);
         case FUSED_SHIFTED:
             if (a.decode_map == 1)

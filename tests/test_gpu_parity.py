@@ -113,12 +113,14 @@ def test_decode_distinct_scales_h7168(mode, T):
 
 
 @pytest.mark.parametrize("mode", ["unshifted", "pre"])
-@pytest.mark.parametrize("T", [1, 5, 33, 64, 113, 128])
+@pytest.mark.parametrize("T", [1, 5, 32, 33, 64, 113, 128])
 def test_decode_sweep_unshifted_h7168(mode, T):
     """Unshifted and pre-only calls of one tile at hidden 7168 (112 slices,
     at most 2 tokens per CTA): the streaming kernel forms the coefficients
-    and the collapse kernel follows. 113 tokens: one more than the slices,
-    so a CTA has two tokens and others one."""
+    and its owner CTAs write the layer input. Up to 64 tokens the fused
+    form's workers take the decode mapping (quarter units up to 32 tokens,
+    whole units above). 113 tokens: one more than the slices, so a CTA has
+    two tokens and others one."""
     d = synth.make_inputs(**synth.decode_workload(T))
     g = run_gpu(mode, d)
     o = run_oracle(mode, d)
