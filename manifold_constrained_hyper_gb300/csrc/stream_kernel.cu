@@ -1052,8 +1052,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                                           __uint_as_float(v[i]) + __uint_as_float(v[24 + i]), pol_keep);
                         st_global_f32(dst + 24 * kTileT, ssq, pol_keep);
                     }
+                    // kept in L2 for the tile's layer-input steps (with the
+                    // default policy these loads missed L2 under the
+                    // streaming load: 1.2 us of a call at 8192 x 7168)
                     if (kShifted)
-                        a.ssql[static_cast<size_t>(it.slice) * a.T + gt] = ssql;
+                        st_global_f32(a.ssql + static_cast<size_t>(it.slice) * a.T + gt, ssql, pol_keep);
                 }
                 // publish this quarter of the item to the tile's other slices
                 // (a single wave: the whole item at once, after the four
@@ -1090,20 +1093,18 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                                            << 16);
                 return __ldg(static_cast<const float *>(a.norm_w) + h);
             };
-            // every chunk's weights (at most 8 chunks) are fetched before the
-            // wait for the tile, off the end of a decode call's critical path,
-            // and parked in this warp's shared copy, so that no registers are
-            // held across the sums of squares below; the lanes then read them
-            // back as broadcasts, four at a time
+            // every chunk's weights (at most 8 chunks) are requested before
+            // the wait for the tile, so that they arrive during it (waiting
+            // for them first cost ~1 us of each layer-input step, 1.7 us of a
+            // call at 8192 x 7168), and are parked in this warp's shared copy
+            // after it, so that no registers are held across the sums of
+            // squares below; the lanes then read them back as broadcasts,
+            // four at a time
             float *nws = red + kNwOff + q * (8 * kChunk);
+            float nwv[8];
             if (kShifted) {
-                float nwv[8];
 #pragma unroll
                 for (int c = 0; c < 8; ++c) nwv[c] = c < d ? nw_lane(c) : 0.f;
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    if (c < d) nws[c * kChunk + lane] = nwv[c];
-                __syncwarp();
             }
             // every slice of the tile published. The layer RMSNorm needs the
             // flags of this warp's token quarter only: one acquire read per
@@ -1155,6 +1156,12 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 // their coefficients (all but the last item's, then the last)
                 if (a.coef_end && kn >= n_local - 2 && ok && lane == 0)
                     mbar_arrive(kn == n_local - 1 ? end_go : prev_go);
+            }
+            if (kShifted) {
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    if (c < d) nws[c * kChunk + lane] = nwv[c];
+                __syncwarp();
             }
             // a captured call of one tile: every CTA has read the cell once this
             // one has seen them all publish; advance it for the next replay
