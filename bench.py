@@ -570,10 +570,17 @@ def run_ours(args):
     cb = torch.empty(T, 4, 4, device=dev)
     ws = torch.empty(max(ops.workspace_bytes(T, H), 16), dtype=torch.uint8, device=dev)
 
+    form = args.form
+
     def step():
-        ops.mhc_boundary_fused(x, res, post, comb, w, scale, base, nw, pre_lag, params,
-                               residual_out=ro, layer_input=li, pre_out=pr, post_out=po,
-                               comb_out=cb, workspace=ws)
+        if form == "pre":
+            ops.mhc_pre(res, w, scale, base, nw, params, layer_input=li, pre_out=pr, post_out=po,
+                        comb_out=cb, workspace=ws)
+        else:
+            ops.mhc_boundary_fused(x, res, post, comb, w, scale, base, nw,
+                                   pre_lag if form == "shifted" else None, params,
+                                   residual_out=ro, layer_input=li, pre_out=pr, post_out=po,
+                                   comb_out=cb, workspace=ws)
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -598,12 +605,15 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    launches0 = ops.mhc_debug_launch_count()
     with ClockSampler(local) as clk:
         t_begin.record()
         for i in range(K):
             step()
         t_end.record()
         torch.cuda.synchronize()
+    # this library's kernels launched in the timed region (counted by the library)
+    gpu_launches = ops.mhc_debug_launch_count() - launches0
     if world > 1:
         dist.barrier()
     status = ops.mhc_get_device_status()
@@ -614,8 +624,11 @@ def run_ours(args):
     ms_per_step = total_ms / K
     value = whole_job_rate(world, T, K, total_ms)
     peak, peak_kind = measured_peaks()
-    gbps_call = alg_bytes_call(T, H) / (ms_per_step / 1e3) / 1e9
-    ach = alg_bytes_stream_kernel(T, H) / (stream_ms / 1e3) / 1e9
+    gbps_call = alg_bytes_form(form, T, H) / (ms_per_step / 1e3) / 1e9
+    # the shifted call is the streaming kernel alone; the other forms are
+    # timed as whole calls (past a single wave: streaming, coefficients and
+    # collapse kernels)
+    ach = alg_bytes_form(form, T, H) / (stream_ms / 1e3) / 1e9
     # the same kernel with events on both sides of each launch (50 launches)
     n_iso = min(K, 50)
     ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(n_iso)]
@@ -636,7 +649,7 @@ def run_ours(args):
     # their own streams, so that step k's copy-out overlaps step k + 1's
     # copy-in (the host link carries both directions at once).
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and form == "shifted":
         K2 = max(1, min(K, args.e2e_steps))
         dev_in = [(torch.empty_like(res), torch.empty_like(x), [torch.empty_like(t) for t in (post, comb, pre_lag)])
                   for _ in range(2)]
@@ -713,14 +726,17 @@ def run_ours(args):
         split_k = measure_split_k(dev)
 
     S, sw = ops.plan(T, H)
-    traffic, traffic_note = stream_kernel_traffic(T, H)
+    traffic, traffic_note = (stream_kernel_traffic(T, H) if form == "shifted"
+                             else (None, "no capture of this form"))
+    variant = {"shifted": "shifted fused boundary", "unshifted": "unshifted fused boundary",
+               "pre": "unshifted pre-only boundary"}[form]
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; residual/x ~ N(0,1) bf16, doubly stochastic comb)",
         "config": {"workload": args.workload, "tokens": T, "hidden": H, "n_hc": 4,
-                   "variant": "shifted fused boundary", "sinkhorn_iters": 20,
+                   "variant": variant, "sinkhorn_iters": 20,
                    "decode_path": "cluster" if ops.plan_cluster(T, H) else "slice-parallel",
                    "norm_w": "fp32", "hidden_slices": S, "slice_width": sw,
                    "l2": "inputs larger than L2 (no flush); prepared mixer L2-resident",
@@ -728,12 +744,14 @@ def run_ours(args):
         "achieved_gbps": gbps_call,
         "achieved_frac_of_peak": gbps_call / peak,
         "kernel_ms": {"stream": stream_ms, "stream_isolated": stream_iso_ms},
-        "roofline": {"bound": "hbm", "kernel": "stream_kernel", "achieved": ach, "peak": peak,
+        "roofline": {"bound": "hbm",
+                     "kernel": "stream_kernel" if form == "shifted" else "whole call",
+                     "achieved": ach, "peak": peak,
                      "unit": "GB/s", "frac": ach / peak, "traffic": traffic,
                      "traffic_source": traffic_note, "peak_source": peak_kind},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K,
+        "gpu_launches": gpu_launches,
         "decode": decode,
         "forms": forms,
         "pre_split_k": split_k,
@@ -752,6 +770,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--form", choices=["shifted", "unshifted", "pre"], default="shifted",
+                    help="the form timed on the workload (the headline is the shifted call; "
+                         "the others for their own roofline and launch lists)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -356,6 +356,12 @@ mhc_status mhc_debug_delayed_copy(const uint16_t *src, uint16_t *dst, int64_t n,
  * does. Other values act as 0. */
 void mhc_debug_set_decode_path(int path);
 
+/* Benchmark hook: the number of kernels this library has launched in the
+ * process so far (every entry point that launches, counted when the launch
+ * succeeded; thread-safe, process-wide, never reset). The difference across
+ * a timed region is the number of the library's kernels in it. */
+uint64_t mhc_debug_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

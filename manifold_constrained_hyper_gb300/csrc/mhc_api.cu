@@ -359,6 +359,14 @@ CoefArgs coef_args(const float *scale, const float *base, const mhc_params *p) {
 
 mhc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
 
+// Kernels this library has launched in the process (mhc_debug_launch_count).
+std::atomic<unsigned long long> g_launches{0};
+// The status of one kernel launch; counts it when it went out.
+mhc_status launched(cudaError_t e) {
+    if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return cuda_status(e);
+}
+
 // Shared body of mhc_pre (x == NULL) and mhc_boundary_fused.
 mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, const float *post,
                         const float *comb, const float *pre_lag, const void *weight,
@@ -431,7 +439,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
             // at least T x 128 bytes there for any plan)
             ca.mix_out = reinterpret_cast<float *>(ws8 + kCellBytes);
             ca.pdl = g_pdl.load();
-            if (mhc_status s = cuda_status(launch_cluster(m_res, m_x, m_rout, ca, st))) return s;
+            if (mhc_status s = launched(launch_cluster(m_res, m_x, m_rout, ca, st))) return s;
             if (t_between_event) {
                 cudaEvent_t ev = t_between_event;
                 t_between_event = nullptr;
@@ -542,7 +550,7 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
             sa.epoch = next_epoch();
         }
     }
-    if (mhc_status s = cuda_status(launch_stream(mode, m_res, m_x, m_rout, sa, S,
+    if (mhc_status s = launched(launch_stream(mode, m_res, m_x, m_rout, sa, S,
                                                  static_cast<int>(items), grid, st)))
         return s;
     if (t_between_event) {
@@ -566,8 +574,8 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     fa.H = H;
     if (mode == FUSED_SHIFTED || sa.collapse_in_kernel) return MHC_OK;
     if (!sa.fuse_coef)
-        if (mhc_status s = cuda_status(launch_coefficients(fa, st))) return s;
-    return cuda_status(launch_collapse_unshifted(fa, st));
+        if (mhc_status s = launched(launch_coefficients(fa, st))) return s;
+    return launched(launch_collapse_unshifted(fa, st));
 }
 
 }  // namespace
@@ -596,7 +604,7 @@ mhc_status mhc_prepare_weight(const float *fn, int hidden, void *weight, void *s
         return MHC_ERR_ALIAS;
     DeviceInfo *dev = nullptr;
     if (mhc_status s = current_device(&dev)) return s;
-    return cuda_status(launch_prepare_weight(fn, hidden, static_cast<uint8_t *>(weight),
+    return launched(launch_prepare_weight(fn, hidden, static_cast<uint8_t *>(weight),
                                              static_cast<cudaStream_t>(stream)));
 }
 
@@ -618,7 +626,7 @@ mhc_status mhc_post(const uint16_t *x, const uint16_t *residual, const float *po
     if (aliasing(outs, 1, ins, 4, residual, residual_out)) return MHC_ERR_ALIAS;
     DeviceInfo *dev = nullptr;
     if (mhc_status s = current_device(&dev)) return s;
-    return cuda_status(launch_post(x, residual, post, comb, residual_out, tokens, hidden,
+    return launched(launch_post(x, residual, post, comb, residual_out, tokens, hidden,
                                    static_cast<cudaStream_t>(stream)));
 }
 
@@ -681,10 +689,10 @@ mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const
     // (latency); many: coefficients for 32 tokens per block, then the
     // collapse (bandwidth)
     if (T <= kSplitKOneKernelTokens && !params->batch_invariant)
-        return cuda_status(launch_pre_split_k(dot_mix, sqrsum, n_splits, fa, st));
-    if (mhc_status s = cuda_status(launch_coefficients_split_k(dot_mix, sqrsum, n_splits, fa, st)))
+        return launched(launch_pre_split_k(dot_mix, sqrsum, n_splits, fa, st));
+    if (mhc_status s = launched(launch_coefficients_split_k(dot_mix, sqrsum, n_splits, fa, st)))
         return s;
-    return cuda_status(launch_collapse_unshifted(fa, st));
+    return launched(launch_collapse_unshifted(fa, st));
 }
 
 mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual, const float *post,
@@ -717,6 +725,8 @@ mhc_status mhc_plan_cluster(int64_t tokens, int hidden, int *ctas) {
 
 void mhc_debug_set_pdl(int enable) { g_pdl.store(enable ? 1 : 0); }
 
+uint64_t mhc_debug_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
 mhc_status mhc_debug_delayed_copy(const uint16_t *src, uint16_t *dst, int64_t n,
                                   uint32_t delay_ns, void *stream) {
     if (n < 0 || delay_ns > 1000000u) return MHC_ERR_SHAPE;
@@ -726,7 +736,7 @@ mhc_status mhc_debug_delayed_copy(const uint16_t *src, uint16_t *dst, int64_t n,
     if (overlap(src, static_cast<size_t>(n) * 2, dst, static_cast<size_t>(n) * 2)) return MHC_ERR_ALIAS;
     DeviceInfo *dev = nullptr;
     if (mhc_status s = current_device(&dev)) return s;
-    return cuda_status(launch_delayed_copy(src, dst, n, delay_ns, static_cast<cudaStream_t>(stream)));
+    return launched(launch_delayed_copy(src, dst, n, delay_ns, static_cast<cudaStream_t>(stream)));
 }
 
 void mhc_debug_set_decode_path(int path) { g_decode_path.store(path == 1 || path == 2 ? path : 0); }
@@ -772,7 +782,7 @@ void mhc_debug_record_between(void *event) {
 mhc_status mhc_debug_unarmed_wait(void *stream) {
     DeviceInfo *dev = nullptr;
     if (mhc_status s = current_device(&dev)) return s;
-    return cuda_status(
+    return launched(
         launch_unarmed_wait(dev->status, g_timeout_ns.load(), static_cast<cudaStream_t>(stream)));
 }
 
@@ -795,7 +805,7 @@ mhc_status mhc_debug_coef_check(const float *values, const float *scale, const f
     if (aliasing(outs, 2, ins, 3, nullptr, nullptr)) return MHC_ERR_ALIAS;
     DeviceInfo *dev = nullptr;
     if (mhc_status s = current_device(&dev)) return s;
-    return cuda_status(launch_coef_check(values, coef_args(scale, base, params), hidden, tokens,
+    return launched(launch_coef_check(values, coef_args(scale, base, params), hidden, tokens,
                                          out_thread, out_lanes, static_cast<cudaStream_t>(stream)));
 }
 
@@ -807,7 +817,7 @@ mhc_status mhc_debug_rcp_check(uint32_t first_bits, uint64_t count, unsigned lon
     if (count > (1ull << 32) - first_bits) return MHC_ERR_SHAPE;
     DeviceInfo *dev = nullptr;
     if (mhc_status s = current_device(&dev)) return s;
-    return cuda_status(launch_rcp_check(first_bits, count, result,
+    return launched(launch_rcp_check(first_bits, count, result,
                                         static_cast<cudaStream_t>(stream)));
 }
 

@@ -28,7 +28,8 @@ EXPORTS = ("mhc_weight_bytes", "mhc_prepare_weight", "mhc_post", "mhc_workspace_
            "mhc_status_string", "mhc_set_wait_timeout_ns", "mhc_debug_unarmed_wait",
            "mhc_plan", "mhc_debug_record_between", "mhc_boundary_fused_noalloc",
            "mhc_debug_rcp_check", "mhc_pre_split_k", "mhc_debug_coef_check", "mhc_plan_cluster",
-           "mhc_debug_set_decode_path", "mhc_debug_set_pdl", "mhc_debug_delayed_copy")
+           "mhc_debug_set_decode_path", "mhc_debug_set_pdl", "mhc_debug_delayed_copy",
+           "mhc_debug_launch_count")
 
 
 class MhcError(RuntimeError):
@@ -99,6 +100,7 @@ def load():
         "mhc_debug_set_decode_path": (None, [i32]),
         "mhc_debug_set_pdl": (None, [i32]),
         "mhc_debug_delayed_copy": (i32, [P, P, i64, ctypes.c_uint32, P]),
+        "mhc_debug_launch_count": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -191,6 +193,11 @@ def mhc_debug_set_pdl(enable: bool):
     """Launch the boundary kernels as programmatic dependents (the default)
     or as plain stream kernels."""
     load().mhc_debug_set_pdl(int(bool(enable)))
+
+
+def mhc_debug_launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load().mhc_debug_launch_count())
 
 
 def mhc_debug_delayed_copy(src, dst, delay_ns: int, stream=None):
