@@ -326,9 +326,10 @@ mhc_status mhc_plan(int64_t tokens, int hidden, int *n_slices, int *slice_width)
  * 64 tokens, params->batch_invariant is 0, its H / 32 chunks split into at
  * most 16 slices of at most 32 chunks and such a cluster can be resident on
  * the device; by default it does so where that is the faster path (a slice
- * of one chunk, or of two chunks for up to 16 tokens: hidden sizes up to
- * 1024; at hidden 7168 the slice-parallel kernel, which spreads the work over
- * 112 CTAs instead of 16, is faster). Cluster calls need no workspace contents (a workspace is
+ * of one chunk; of two chunks for up to 32 tokens; of up to four chunks for
+ * up to 16 tokens: hidden sizes up to 2048; at hidden 7168 the slice-parallel
+ * kernel, which spreads the work over 112 CTAs instead of 16, is faster).
+ * Cluster calls need no workspace contents (a workspace is
  * still passed and checked); after the call its bytes 256 .. 256 + 112 T
  * hold each token's 24 mixes and 4H sum of squares as 28 fp32 (the last
  * three zero). Queries the device once per shape. */

@@ -281,14 +281,16 @@ std::atomic<int> g_pdl{1};
 // wherever one fits (test and benchmark hooks).
 std::atomic<int> g_decode_path{0};
 
-// Where the cluster kernel is the faster (measured, graph replay at 1 to 64
-// tokens and hidden 256 to 7168 against the slice-parallel streaming kernel):
-// when each CTA streams one chunk (by 1.4-4.3 us), or two chunks for up to 16
-// tokens (by ~0.8 us). With more chunks per CTA its 16 CTAs carry 4-14 times
-// the per-SM work of the slice-parallel kernel (weight tiles pulled from L2,
-// elementwise chains, MMA instructions) and lose.
+// Where the cluster kernel is the faster (measured on one box, graph replay
+// at 1 to 64 tokens and hidden 512 to 4096 against the slice-parallel
+// streaming kernel): when each CTA streams one chunk (by 0.9-2.2 us), two
+// chunks for up to 32 tokens (by 0.2-1.7 us), up to four for up to 16 tokens
+// (hidden 2048: by 1.0 us at 1 to 8 tokens, 0.25 us at 16). With more chunks
+// per CTA its 16 CTAs carry 4-14 times the per-SM work of the slice-parallel
+// kernel (weight tiles pulled from L2, elementwise chains, MMA instructions)
+// and lose (hidden 4096: even at 1 to 4 tokens, worse from 8).
 bool cluster_preferred(long long T, const ClusterArgs &ca) {
-    return ca.nch == 1 || (ca.nch == 2 && T <= 16);
+    return ca.nch == 1 || (ca.nch == 2 && T <= 32) || (ca.nch <= 4 && T <= 16);
 }
 
 // The shifted call of at most kClusterMaxTokens tokens on one thread-block

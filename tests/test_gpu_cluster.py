@@ -193,15 +193,20 @@ def test_cluster_calls_capture_and_replay_with_new_inputs(T):
 
 def test_default_path_choice():
     """By default the cluster kernel takes the shapes where it is the faster
-    path: one chunk per CTA, or two for up to 16 tokens."""
+    path: one chunk per CTA, two for up to 32 tokens, up to four for up to
+    16 tokens."""
     ops.mhc_debug_set_decode_path(0)
     try:
         assert ops.plan_cluster(1, 256) == 8 and ops.plan_cluster(64, 512) == 16
-        assert ops.plan_cluster(8, 1024) == 16 and ops.plan_cluster(17, 1024) == 0
-        assert ops.plan_cluster(1, 7168) == 0 and ops.plan_cluster(64, 4096) == 0
-        d = synth.make_inputs(5, 512, seed=1900)
-        g = run_gpu("shifted", d)
-        assert g["path"] == "cluster"
-        compare("shifted", g, run_oracle("shifted", d))
+        assert ops.plan_cluster(32, 1024) == 16 and ops.plan_cluster(33, 1024) == 0
+        assert ops.plan_cluster(16, 2048) == 16 and ops.plan_cluster(17, 2048) == 0
+        assert ops.plan_cluster(1, 4096) == 0 and ops.plan_cluster(1, 7168) == 0
+        assert ops.plan_cluster(64, 4096) == 0
+        for T, H, path in [(5, 512, "cluster"), (32, 1024, "cluster"), (16, 2048, "cluster"),
+                           (17, 2048, "slices")]:
+            d = synth.make_inputs(T, H, seed=1900 + T + H)
+            g = run_gpu("shifted", d)
+            assert g["path"] == path
+            compare("shifted", g, run_oracle("shifted", d))
     finally:
         ops.mhc_debug_set_decode_path(2)
