@@ -368,13 +368,15 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     ++loaded;
                 }
             }
-            bulk_wait_all();
+            bulk_wait_read_all();
             if (g < total) {  // aborted: let the loads in flight land before exiting
                 for (int c = g; c < loaded; ++c)
                     drain_wait(full(c % kStages), (c / kStages) & 1, tmo, a.status);
             }
-            // the stage buffers are free of this CTA's copies
+            // the stage buffers are free of this CTA's copies (the stores
+            // have read them; their writes complete below)
             if (kShifted && a.coef_end) mbar_arrive(stages_free);
+            bulk_wait_all();
         } else if (warp == 1 && lane == 0 && !kDecodeMap) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t kIdesc = idesc_bf16_f32(kTileT, kWRows);
@@ -651,20 +653,25 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
 
         // ---- several items per CTA: the coefficients of every token of the
         // CTA's items, formed by the workers once they have streamed their
-        // last chunk and the producer's copies have left the stage buffers
-        // (free from then on): first those of items 0..n-2, whose tiles have
-        // long published by then (prev_go), then those of the last item once
-        // its tile has too (end_go), so that little is left for the end of
-        // the kernel. Nothing of this runs while the CTA streams. Token groups
-        // of 4 (tokens 4gi..4gi+3 of an item's tile, gi = slice, slice + S,
-        // ...) go in rounds of up to kEndGroups: one bulk copy per group lands
-        // its partial records [4 tokens][S slices][32] (contiguous in the
-        // workspace) in its slot of the stage area, all in flight at once; a
-        // thread per (group, token, value) sums over the slices in slice
-        // order (a running sum from zero, as every other path) and leaves the
-        // sum in place; then a thread per token forms pre / post / comb.
-        // Worker thread 0 lays out each round in shared memory, so every
-        // worker warp takes part in each barrier, also after an abort.
+        // last chunk and the producer's stores have read the stage buffers
+        // (free from then on). Nothing of this runs while the CTA streams.
+        // Token groups of 4 (tokens 4gi..4gi+3 of an item's tile, gi = slice,
+        // slice + S, ...) go in rounds of up to kEndGroups: one bulk copy per
+        // group lands its partial records [4 tokens][S slices][32] (contiguous
+        // in the workspace) in its slot of the stage area; a thread per
+        // (group, token, value) sums over the slices in slice order (a running
+        // sum from zero, as every other path) and leaves the sum in place;
+        // then a thread per token forms pre / post / comb. The groups of
+        // items 0..n_early-1 (all but the last two items, or but the last one
+        // for two items), whose tiles the finishers have seen published by
+        // then (prev_go), are copied at once; those of the later items are
+        // laid out in the same round where they fit and copied as soon as the
+        // last tile has published (end_go), while the first copies are in
+        // flight, so that one coefficient step serves both (a separate round
+        // for the last item, gated on item n-2, left two in series: 1.7 us
+        // more at 8192 x 7168, 4.4 us at 2048). Worker thread 0 lays out each
+        // round in shared memory, so every worker warp takes part in each
+        // barrier, also after an abort.
         if (kShifted && a.coef_end) {
             const int wt = tid - 4 * 32;                   // 0..255 among the workers
             bool ok = g == total && mbar_wait(stages_free, 0, abort_flag, tmo, a.status, SITE_WORK_COEF);
@@ -676,21 +683,23 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
             int per_round = static_cast<int>((kStages * kStageBytes) / slot);
             if (per_round > kEndGroups) per_round = kEndGroups;
             const uint64_t pol_once = policy_evict_first();
+            // items [0, n_early) wait for prev_go, the rest for end_go
+            const int n_early = n_local >= 3 ? n_local - 2 : n_local - 1;
+            if (n_early > 0)
+                ok = ok && mbar_wait(prev_go, 0, abort_flag, tmo, a.status, SITE_WORK_COEF);
+            ok = workers_and(ok);
+            bool late_seen = false;                        // end_go waited for
             int ck = 0, cg = item_of(0, n_slices).slice;   // thread 0: next (item, group)
             uint32_t round = 0;
-            for (int phase = 0; phase < 2; ++phase) {
-                // phase 0: items [0, n_local - 1); phase 1: the last item
-                const int k_end = phase == 0 ? n_local - 1 : n_local;
-                if (phase == 0 && k_end <= 0) continue;
-                const uint32_t go = phase == 0 ? prev_go : end_go;
-                ok = __all_sync(0xffffffffu, ok && mbar_wait(go, 0, abort_flag, tmo, a.status, SITE_WORK_COEF));
+            {
                 for (;; ++round) {
                     if (wt == 0) {
-                        int n = 0;
-                        while (ok && n < per_round && ck < k_end) {
+                        int n = 0, n_a = -1;
+                        while (ok && n < per_round && ck < n_local) {
                             const Item it = item_of(ck, n_slices);
                             if (cg < kTileT / kCoefGroup &&
                                 static_cast<long long>(it.tile) * kTileT + kCoefGroup * cg < a.T) {
+                                if (ck >= n_early && n_a < 0) n_a = n;
                                 rdesc[1 + 2 * n] = it.tile;
                                 rdesc[2 + 2 * n] = cg;
                                 ++n;
@@ -700,20 +709,33 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                             }
                         }
                         rdesc[0] = n;
+                        rdesc[200] = n_a < 0 ? n : n_a;
                         if (n > 0) mbar_arrive_expect_tx(end_full, n * grp_bytes);
                     }
                     named_barrier_sync(kWorkBarrier, kWorkThreads);
-                    const int n = rdesc[0];
+                    const int n = rdesc[0], n_a = rdesc[200];
                     named_barrier_sync(kWorkBarrier, kWorkThreads);   // rdesc[0] read by all
                     if (n == 0) break;
-                    if (wt < n) {
-                        // the records were written by other CTAs' generic
-                        // stores, acquired through the finishers (prev_go, end_go)
-                        const long long t0 = static_cast<long long>(rdesc[1 + 2 * wt]) * kTileT +
-                                             kCoefGroup * rdesc[2 + 2 * wt];
+                    // the records were written by other CTAs' generic stores,
+                    // acquired through the finishers (prev_go, end_go); the
+                    // groups of the last items go out once their tiles have
+                    // published, while the earlier groups' copies are in flight
+                    auto copy_group = [&](int i) {
+                        const long long t0 = static_cast<long long>(rdesc[1 + 2 * i]) * kTileT +
+                                             kCoefGroup * rdesc[2 + 2 * i];
                         fence_proxy_async_global();
-                        bulk_load(base + wt * slot, a.partials + t0 * n_slices * kRecFloats, grp_bytes,
+                        bulk_load(base + i * slot, a.partials + t0 * n_slices * kRecFloats, grp_bytes,
                                   end_full, pol_once);
+                    };
+                    if (wt < n_a) copy_group(wt);
+                    if (n_a < n) {
+                        if (!late_seen) {
+                            ok = workers_and(ok && mbar_wait(end_go, 0, abort_flag, tmo, a.status,
+                                                             SITE_WORK_COEF));
+                            late_seen = true;
+                        }
+                        // (after an abort too: the expected bytes must land)
+                        if (wt >= n_a && wt < n) copy_group(wt);
                     }
                     // the copies must land before the buffers are read or the
                     // CTA exits: a bounded wait that ignores aborts
@@ -946,16 +968,22 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // published too. In the order P0 P1 L0 P2 L1 ... P(n-2) L(n-3), an
         // item's siblings have almost always published by the time of its
         // L step, so the polls rarely wait (polling right after each P cost
-        // 10 % of a long run). The tail runs L(n-2) P(n-1) L(n-1): L(n-2)
-        // then overlaps the streaming of the last item, and only L(n-1) is
-        // left after its last chunk. Every wait points at an earlier tile or
+        // 10 % of a long run). With three or more items the tail runs
+        // P(n-1) L(n-2) L(n-1): the layer-input steps take most of an item's
+        // time in a long call, so L(n-2) could not overlap the last item's
+        // streaming and held its publication ~5 us after its last chunk.
+        // With two items it runs L0 P1 L1, so that L0 overlaps item 1's
+        // streaming (measured 2.3 us faster at 1024 tokens). Every wait points at an earlier tile or
         // at items the same wave streams without this CTA, so there is no
         // cycle. Iteration j runs P(pk) (if pk >= 0), then L(lk) (if lk >= 0);
         // the decode variants (one item) run P0 L0 in one iteration.
         const int n_iter = kDecodeMap ? 1 : n_local + 1;
         for (int j = 0; j < n_iter; ++j) {
-            const int pk = kDecodeMap ? 0 : j < n_local - 1 ? j : (j == n_local ? n_local - 1 : -1);
-            const int lk = kDecodeMap ? 0 : j < n_local ? j - 1 : n_local - 1;
+            const bool tail_p_first = n_local >= 3;
+            const int pk = kDecodeMap ? 0
+                                      : tail_p_first ? (j < n_local ? j : -1)
+                                                     : j < n_local - 1 ? j : (j == n_local ? n_local - 1 : -1);
+            const int lk = kDecodeMap ? 0 : tail_p_first ? j - 1 : j < n_local ? j - 1 : n_local - 1;
             if (pk >= 0) {
                 const int k = pk;
                 const int b = k % kAccBufs;
@@ -1154,8 +1182,11 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 // the tiles of items 0..kn have all published in full (each
                 // finisher warp saw its quarter of each): the workers may form
                 // their coefficients (all but the last item's, then the last)
-                if (a.coef_end && kn >= n_local - 2 && ok && lane == 0)
-                    mbar_arrive(kn == n_local - 1 ? end_go : prev_go);
+                if (a.coef_end && ok && lane == 0) {
+                    const int n_early = n_local >= 3 ? n_local - 2 : n_local - 1;
+                    if (kn == n_local - 1) mbar_arrive(end_go);
+                    else if (kn == n_early - 1) mbar_arrive(prev_go);
+                }
             }
             if (kShifted) {
 #pragma unroll
