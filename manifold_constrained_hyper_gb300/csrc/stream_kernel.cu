@@ -666,8 +666,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
         // for two items), whose tiles the finishers have seen published by
         // then (prev_go), are copied at once; those of the later items are
         // laid out in the same round where they fit and copied as soon as the
-        // last tile has published (end_go), while the first copies are in
-        // flight, so that one coefficient step serves both (a separate round
+        // last tiles have published (polled by the workers; end_go for two
+        // items), while the first copies are in flight, so that one
+        // coefficient step serves both (a separate round
         // for the last item, gated on item n-2, left two in series: 1.7 us
         // more at 8192 x 7168, 4.4 us at 2048). Worker thread 0 lays out each
         // round in shared memory, so every worker warp takes part in each
@@ -729,6 +730,42 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     };
                     if (wt < n_a) copy_group(wt);
                     if (n_a < n) {
+                        if (!late_seen && n_local >= 3) {
+                            // the last items' tiles: every slice's quarter
+                            // flags, polled by the workers themselves (the
+                            // finishers see them only after L(n-2): 1.5 us
+                            // later at 8192 x 7168); the flag value came
+                            // with prev_go. (Two items: end_go, measured
+                            // 0.3 us faster at 1024 tokens.)
+                            const unsigned long long ep =
+                                *reinterpret_cast<volatile const unsigned long long *>(gbase + kMiscOff + 48);
+                            const int per_tile = n_slices * 4;
+                            const int nt = (n_local - n_early) * per_tile;
+                            uint64_t t_start = 0;
+                            for (;;) {
+                                bool seen = true;
+                                for (int i = wt; i < nt; i += kWorkThreads) {
+                                    const Item itk = item_of(n_early + i / per_tile, n_slices);
+                                    seen = seen && flag_acquire(a.flags + static_cast<long long>(itk.tile) * per_tile +
+                                                                i % per_tile) == ep;
+                                }
+                                if (workers_and(seen)) break;
+                                if (!workers_and(!*abort_flag)) { ok = false; break; }
+                                const uint64_t now = globaltimer_ns();
+                                if (t_start == 0) t_start = now;
+                                if (!workers_and(now - t_start <= tmo)) {
+                                    if (wt == 0) {
+                                        record_failure(a.status, 7, SITE_WORK_COEF);
+                                        *abort_flag = 1;
+                                    }
+                                    ok = false;
+                                    break;
+                                }
+                                nanosleep_ns(200);
+                            }
+                            ok = workers_and(ok);
+                            late_seen = true;
+                        }
                         if (!late_seen) {
                             ok = workers_and(ok && mbar_wait(end_go, 0, abort_flag, tmo, a.status,
                                                              SITE_WORK_COEF));
