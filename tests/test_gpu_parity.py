@@ -164,6 +164,23 @@ def test_shifted_several_items_per_cta(T, H):
     compare("shifted", g, o, d=d)
 
 
+@pytest.mark.parametrize("T", [385, 513])
+def test_end_rounds_split_around_the_last_items(T):
+    """Hidden 38912 plans 152 slices of 256, so a token group's records take
+    over a third of the stage area and an end-of-call round holds two groups;
+    CTAs 0-31 have one group per item and 4 (385 tokens) or 5 (513) items.
+    The last two items' groups, copied once their tiles have published, then
+    fill a later round on their own (4 items) or share one with an earlier
+    item's group (5 items: a round straddles the two kinds)."""
+    H = 38912
+    S, _ = ops.plan(T, H)
+    assert S == 152 and (T + 127) // 128 in (4, 5)
+    d = synth.make_inputs(T, H, seed=760 + T)
+    g = run_gpu("shifted", d)
+    o = run_oracle("shifted", d)
+    compare("shifted", g, o, d=d)
+
+
 @pytest.mark.parametrize("scale", [(0.5, 0.5, 0.5), DISTINCT_SCALES])
 @pytest.mark.parametrize("mode", ["pre", "unshifted", "shifted"])
 def test_mid_batch_t512_h7168(mode, scale):
