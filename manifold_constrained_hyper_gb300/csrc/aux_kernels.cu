@@ -140,6 +140,9 @@ __global__ void __launch_bounds__(kCoefThreads, 2) coefficients_kernel(const Fin
     if (warp == 0 && t < a.T)
         coefficients_thread(&red[0][lane], kCoefTokens, consts, a.coef, a.H, t, a.pre_out,
                             a.post_out, a.comb_out);
+    // a collapse kernel launched as this kernel's programmatic dependent may
+    // start once every block has written its tokens' coefficients
+    griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------ coefficients (split-K)
@@ -289,6 +292,8 @@ __global__ void __launch_bounds__(kColThreads) collapse_unshifted_kernel(const F
     // last tokens first: the streaming pass touched them last, so part of
     // their rows is still in L2
     const long long t = a.T - 1 - blockIdx.x;
+    // (a no-op unless launched as a programmatic dependent)
+    griddep_wait();
     const float4 pv = reinterpret_cast<const float4 *>(a.pre_out)[t];
     const uint64_t p2[4] = {f2_pack(pv.x, pv.x), f2_pack(pv.y, pv.y), f2_pack(pv.z, pv.z),
                             f2_pack(pv.w, pv.w)};
@@ -479,12 +484,21 @@ cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_
     return cudaGetLastError();
 }
 
-cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s) {
+cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool pdl) {
     const size_t smem = static_cast<size_t>(a.H) * 2;
     if (cudaError_t e = ensure_dynamic_smem(collapse_unshifted_kernel, g_optin_collapse, smem))
         return e;
-    collapse_unshifted_kernel<<<static_cast<unsigned>(a.T), kColThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.T));
+    cfg.blockDim = dim3(kColThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, collapse_unshifted_kernel, a);
 }
 
 // Test hook: the coefficients of n tokens from reduced values v [n][25],

@@ -577,7 +577,16 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     if (mode == FUSED_SHIFTED || sa.collapse_in_kernel) return MHC_OK;
     if (!sa.fuse_coef)
         if (mhc_status s = launched(launch_coefficients(fa, st))) return s;
-    return launched(launch_collapse_unshifted(fa, st));
+    // after the coefficients kernel, as its programmatic dependent (released
+    // once every block has written its coefficients) for pre-only calls of up
+    // to 2048 tokens and unshifted ones of up to 512: at hidden 7168 1.2-2.2
+    // us less per pre-only call from 512 to 2048 tokens and 2.5 us less per
+    // unshifted call at 512, but 0.3-0.7 us more per unshifted call at 1024
+    // and 2048, and 4-12 us more per call at 8192. Directly after the
+    // streaming kernel (which releases its dependents at its start) a plain
+    // launch.
+    const bool pdl_collapse = !sa.fuse_coef && T <= (mode == PRE_ONLY ? 2048 : 512);
+    return launched(launch_collapse_unshifted(fa, st, pdl_collapse));
 }
 
 }  // namespace
@@ -694,7 +703,7 @@ mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const
         return launched(launch_pre_split_k(dot_mix, sqrsum, n_splits, fa, st));
     if (mhc_status s = launched(launch_coefficients_split_k(dot_mix, sqrsum, n_splits, fa, st)))
         return s;
-    return launched(launch_collapse_unshifted(fa, st));
+    return launched(launch_collapse_unshifted(fa, st, false));
 }
 
 mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual, const float *post,

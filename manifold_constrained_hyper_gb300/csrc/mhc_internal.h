@@ -167,7 +167,9 @@ cudaError_t launch_cluster(const CUtensorMap &res, const CUtensorMap &x, const C
 // Whether a cluster of `ctas` CTAs with `smem` bytes of dynamic shared memory
 // can be resident on the current device (checked once per size and device).
 bool cluster_fits(int ctas, uint32_t smem);
-cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s);
+// pdl: as a programmatic dependent of the kernel before it (which must
+// release it only once the pre it reads is written)
+cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool pdl);
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
                                const FinishArgs &a, cudaStream_t s);

@@ -6,7 +6,9 @@ start at once and writes the residual only 20 us later stands in for the
 layer kernel before the boundary; the boundary after it, eager and replayed
 from a CUDA graph, must give bit for bit the results of a call on the
 finished residual. Covers the slice-parallel decode and multi-item kernels,
-the cluster kernel, and the unshifted forms."""
+the cluster kernel, and the unshifted forms (among them the collapse kernel
+as a programmatic dependent of the coefficients kernel: pre-only up to 2048
+tokens, unshifted up to 512)."""
 import numpy as np
 import pytest
 import torch
@@ -31,8 +33,9 @@ def _bits(t):
 
 @pytest.mark.parametrize("form,T,H", [("shifted", 1, 7168), ("shifted", 64, 7168),
                                       ("shifted", 2048, 7168), ("shifted", 5, 512),
-                                      ("unshifted", 8, 7168), ("unshifted", 700, 4096),
-                                      ("pre", 1, 7168), ("pre", 512, 7168)])
+                                      ("unshifted", 8, 7168), ("unshifted", 300, 7168),
+                                      ("unshifted", 700, 4096), ("pre", 1, 7168), ("pre", 512, 7168),
+                                      ("pre", 1500, 4096)])
 def test_boundary_after_a_late_producer(form, T, H):
     d = synth.make_inputs(T, H, seed=2000 + T + H)
     res_src = dev_bf16(d["residual"])
