@@ -181,6 +181,9 @@ coefficients_split_k_kernel(const float *__restrict__ dot_mix, const float *__re
     if (warp == 0 && t0 + lane < a.T)
         coefficients_thread(&red[0][lane], kCoefTokens, consts, a.coef, a.H, t0 + lane, a.pre_out,
                             a.post_out, a.comb_out);
+    // the collapse kernel after it (a programmatic dependent) may start once
+    // every block has written its tokens' coefficients
+    griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------ split-K pre, one kernel

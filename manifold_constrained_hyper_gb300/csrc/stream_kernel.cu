@@ -175,9 +175,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
     const uint32_t exit_bar = bars + 8u * (3 * kStages + 4 * kAccBufs + kLiBufs);   // every warp is done
     const uint32_t coef_go = exit_bar + 8u;   // single wave: the tile's partials are all published
     // several items: the producer's copies have left the stage buffers;
-    // every finisher warp has seen the tile of the CTA's last item but one
-    // (prev_go) and of its last item (end_go) published; a round's partial
-    // records have landed (end_full)
+    // every finisher warp has seen the tiles of the CTA's items
+    // 0..n_early-1 (prev_go) and of its last item (end_go) published; a
+    // round's partial records have landed (end_full)
     const uint32_t stages_free = coef_go + 8u;
     const uint32_t prev_go = stages_free + 8u;
     const uint32_t end_go = prev_go + 8u;
@@ -718,9 +718,10 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                     named_barrier_sync(kWorkBarrier, kWorkThreads);   // rdesc[0] read by all
                     if (n == 0) break;
                     // the records were written by other CTAs' generic stores,
-                    // acquired through the finishers (prev_go, end_go); the
-                    // groups of the last items go out once their tiles have
-                    // published, while the earlier groups' copies are in flight
+                    // acquired through the finishers (prev_go, end_go) or the
+                    // workers' own polls; the groups of the last items go out
+                    // once their tiles have published, while the earlier
+                    // groups' copies are in flight
                     auto copy_group = [&](int i) {
                         const long long t0 = static_cast<long long>(rdesc[1 + 2 * i]) * kTileT +
                                              kCoefGroup * rdesc[2 + 2 * i];
@@ -1217,8 +1218,9 @@ stream_kernel(const __grid_constant__ CUtensorMap tm_res, const __grid_constant_
                 if (a.fuse_coef && q == 0) fence_acq_rel_gpu();
                 __syncwarp();
                 // the tiles of items 0..kn have all published in full (each
-                // finisher warp saw its quarter of each): the workers may form
-                // their coefficients (all but the last item's, then the last)
+                // finisher warp saw its quarter of each): the workers may
+                // copy those items' partial records (prev_go: items
+                // 0..n_early-1; end_go: every item)
                 if (a.coef_end && ok && lane == 0) {
                     const int n_early = n_local >= 3 ? n_local - 2 : n_local - 1;
                     if (kn == n_local - 1) mbar_arrive(end_go);
