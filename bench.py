@@ -247,6 +247,8 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
+    if args.form != "shifted":
+        raise SystemExit("bench: --impl reference times the shifted call only")
     from manifold_constrained_hyper_gb300 import synth
     import oracle as orc
     orc.build_oracle()
