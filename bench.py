@@ -9,8 +9,8 @@ than L2 (129 MB), so no flush is needed; the prepared mixer (2.75 MB) stays
 L2-resident as it does in a serving loop.
 
 Prints one JSON line (rank 0). --impl reference times the CPU oracle instead
-(this build has no other reference implementation), on a bounded sample of
-the same workload.
+(there is no other reference implementation), on a bounded sample of the
+same workload.
 """
 from __future__ import annotations
 
