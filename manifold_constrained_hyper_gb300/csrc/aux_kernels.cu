@@ -192,13 +192,17 @@ coefficients_split_k_kernel(const float *__restrict__ dot_mix, const float *__re
 // hands pre to warps 1-3, which collapse the token's 4 streams with it and
 // write the RMS-normed layer input ("computing pre_mix early" on the page:
 // the collapse needs pre only); meanwhile lane 0 of warp 0 forms post and
-// the Sinkhorn comb. Same arithmetic and order as the two-kernel form.
-constexpr int kSkThreads = 128;
-constexpr int kSkCollapse = kSkThreads - 32;
-
-__global__ void __launch_bounds__(kSkThreads)
+// the Sinkhorn comb. The coefficients' arithmetic and order are the
+// two-kernel form's; the collapse's sum of squares is reduced in this
+// kernel's own fixed order. THREADS: 128, or 512 when every token has an SM
+// to itself (the collapse's loads then come from 15 warps instead of 3:
+// 6.75 -> 4.94 us at 128 tokens, hidden 7168; with more tokens than SMs the
+// wide blocks measured slower, 10.6 against 8.3 us at 512 tokens).
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
 pre_split_k_kernel(const float *__restrict__ dot_mix, const float *__restrict__ sqrsum,
                    int n_splits, const FinishArgs a) {
+    constexpr int kSkCollapse = THREADS - 32;
     extern __shared__ uint4 li_s[];            // [H/8]
     __shared__ float vals[kPartVals];
     __shared__ float consts[32];
@@ -408,7 +412,7 @@ cudaError_t ensure_dynamic_smem(K kernel, SmemOptIn &opt, size_t smem) {
     return cudaSuccess;
 }
 
-SmemOptIn g_optin_split_k, g_optin_collapse;
+SmemOptIn g_optin_split_k, g_optin_split_k_wide, g_optin_collapse;
 
 unsigned int *device_status_word() {
     void *p = nullptr;
@@ -479,11 +483,19 @@ cudaError_t launch_coefficients_split_k(const float *dot_mix, const float *sqrsu
 }
 
 cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
-                               const FinishArgs &a, cudaStream_t s) {
+                               const FinishArgs &a, cudaStream_t s, bool wide) {
     const size_t smem = static_cast<size_t>(a.H) * 2;
-    if (cudaError_t e = ensure_dynamic_smem(pre_split_k_kernel, g_optin_split_k, smem)) return e;
-    pre_split_k_kernel<<<static_cast<unsigned>(a.T), kSkThreads, smem, s>>>(dot_mix, sqrsum,
-                                                                          n_splits, a);
+    if (wide) {
+        if (cudaError_t e = ensure_dynamic_smem(pre_split_k_kernel<512>, g_optin_split_k_wide, smem))
+            return e;
+        pre_split_k_kernel<512><<<static_cast<unsigned>(a.T), 512, smem, s>>>(dot_mix, sqrsum,
+                                                                              n_splits, a);
+    } else {
+        if (cudaError_t e = ensure_dynamic_smem(pre_split_k_kernel<128>, g_optin_split_k, smem))
+            return e;
+        pre_split_k_kernel<128><<<static_cast<unsigned>(a.T), 128, smem, s>>>(dot_mix, sqrsum,
+                                                                              n_splits, a);
+    }
     return cudaGetLastError();
 }
 

@@ -700,7 +700,7 @@ mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const
     // (latency); many: coefficients for 32 tokens per block, then the
     // collapse (bandwidth)
     if (T <= kSplitKOneKernelTokens && !params->batch_invariant)
-        return launched(launch_pre_split_k(dot_mix, sqrsum, n_splits, fa, st));
+        return launched(launch_pre_split_k(dot_mix, sqrsum, n_splits, fa, st, T <= dev->sms));
     if (mhc_status s = launched(launch_coefficients_split_k(dot_mix, sqrsum, n_splits, fa, st)))
         return s;
     // as a programmatic dependent of the coefficients kernel (released after

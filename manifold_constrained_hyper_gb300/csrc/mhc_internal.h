@@ -171,8 +171,9 @@ bool cluster_fits(int ctas, uint32_t smem);
 // release it only once the pre it reads is written)
 cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool pdl);
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
+// wide: 512 threads per token (every token on an SM of its own), else 128
 cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
-                               const FinishArgs &a, cudaStream_t s);
+                               const FinishArgs &a, cudaStream_t s, bool wide);
 cudaError_t launch_coefficients_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
                                         const FinishArgs &a, cudaStream_t s);
 cudaError_t launch_prepare_weight(const float *fn, int H, uint8_t *out, cudaStream_t s);

@@ -40,7 +40,7 @@ def check(d, g, norm="f32"):
 
 
 @pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
-@pytest.mark.parametrize("T,H", [(1, 7168), (37, 256), (129, 4096)])
+@pytest.mark.parametrize("T,H", [(1, 7168), (37, 256), (129, 4096), (300, 7168), (1024, 512)])
 def test_split_k_pre_parity(S, T, H):
     d = synth.make_split_k_inputs(T, H, S, seed=700 + T + S)
     check(d, run_split_k(d))
