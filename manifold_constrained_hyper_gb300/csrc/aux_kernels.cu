@@ -290,9 +290,11 @@ pre_split_k_kernel(const float *__restrict__ dot_mix, const float *__restrict__ 
 // token's 4 updated streams with this boundary's pre into shared memory,
 // reduce the collapse's sum of squares in a fixed order, and write the
 // normalised layer input.
-constexpr int kColThreads = 128;
-
-__global__ void __launch_bounds__(kColThreads) collapse_unshifted_kernel(const FinishArgs a) {
+// THREADS: 128, or 512 when every token has an SM of its own (a few tokens
+// after a single wave: the loads then come from 16 warps instead of 4).
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) collapse_unshifted_kernel(const FinishArgs a) {
+    constexpr int kColThreads = THREADS;
     extern __shared__ uint4 li_s[];            // [H/8]
     __shared__ float red_s[kColThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -412,7 +414,7 @@ cudaError_t ensure_dynamic_smem(K kernel, SmemOptIn &opt, size_t smem) {
     return cudaSuccess;
 }
 
-SmemOptIn g_optin_split_k, g_optin_split_k_wide, g_optin_collapse;
+SmemOptIn g_optin_split_k, g_optin_split_k_wide, g_optin_collapse, g_optin_collapse_wide;
 
 unsigned int *device_status_word() {
     void *p = nullptr;
@@ -499,13 +501,14 @@ cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_
     return cudaGetLastError();
 }
 
-cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool pdl) {
+cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool pdl, bool wide) {
     const size_t smem = static_cast<size_t>(a.H) * 2;
-    if (cudaError_t e = ensure_dynamic_smem(collapse_unshifted_kernel, g_optin_collapse, smem))
+    auto kern = wide ? collapse_unshifted_kernel<512> : collapse_unshifted_kernel<128>;
+    if (cudaError_t e = ensure_dynamic_smem(kern, wide ? g_optin_collapse_wide : g_optin_collapse, smem))
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.T));
-    cfg.blockDim = dim3(kColThreads);
+    cfg.blockDim = dim3(wide ? 512 : 128);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -513,7 +516,7 @@ cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, collapse_unshifted_kernel, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // Test hook: the coefficients of n tokens from reduced values v [n][25],

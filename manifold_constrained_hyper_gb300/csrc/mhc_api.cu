@@ -586,7 +586,9 @@ mhc_status run_boundary(int mode, const uint16_t *x, const uint16_t *residual, c
     // streaming kernel (which releases its dependents at its start) a plain
     // launch.
     const bool pdl_collapse = !sa.fuse_coef && T <= (mode == PRE_ONLY ? 2048 : 512);
-    return launched(launch_collapse_unshifted(fa, st, pdl_collapse));
+    // (batch-invariant calls keep one block size, so that the collapse's sum
+    // of squares has one order at every batch size)
+    return launched(launch_collapse_unshifted(fa, st, pdl_collapse, !invariant && T <= dev->sms));
 }
 
 }  // namespace
@@ -706,7 +708,7 @@ mhc_status mhc_pre_split_k(const uint16_t *residual, const float *dot_mix, const
     // as a programmatic dependent of the coefficients kernel (released after
     // its coefficients): 0.66 us less at 1536 x 4096, 0.35 at 2048 x 7168,
     // unchanged at 4096 tokens
-    return launched(launch_collapse_unshifted(fa, st, true));
+    return launched(launch_collapse_unshifted(fa, st, true, !params->batch_invariant && T <= dev->sms));
 }
 
 mhc_status mhc_boundary_fused(const uint16_t *x, const uint16_t *residual, const float *post,

@@ -169,7 +169,8 @@ cudaError_t launch_cluster(const CUtensorMap &res, const CUtensorMap &x, const C
 bool cluster_fits(int ctas, uint32_t smem);
 // pdl: as a programmatic dependent of the kernel before it (which must
 // release it only once the pre it reads is written)
-cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool pdl);
+// wide: 512 threads per token (every token on an SM of its own), else 128
+cudaError_t launch_collapse_unshifted(const FinishArgs &a, cudaStream_t s, bool pdl, bool wide);
 cudaError_t launch_coefficients(const FinishArgs &a, cudaStream_t s);
 // wide: 512 threads per token (every token on an SM of its own), else 128
 cudaError_t launch_pre_split_k(const float *dot_mix, const float *sqrsum, int n_splits,
